@@ -1,0 +1,376 @@
+"""Benchmark: one decode-maximal hybrid batch through the LLaMA-13B layer.
+
+Workload (one step): a prefill chunk of 256 tokens at offset 768 of a
+1024-token prompt plus 18 decodes at context 1024, T = 274 rows, through one
+LLaMA-13B decoder layer (hidden 5120, 40 heads x 128, SwiGLU FFN 13824),
+bf16 weights ~N(0, 0.02), KV cache ~N(0, 1) in shuffled 16-token blocks.
+Every step writes the batch's K/V and reads 399 MB of KV plus 634 MB of
+weights, far more than the 126 MB L2, so no L2 flush is needed between steps.
+
+Reported (one JSON line on rank 0):
+  value      hybrid-batch tokens/s (T x steps / device time), inputs resident
+  e2e        the same through hb_forward_host: pinned host x in, host y out
+  decode     decode tok/s piggybacked (marginal over the chunk alone, the
+             pages' definition) vs in a decode-only batch of the same 18
+  roofline   the dominant kernel against MEASURED_PEAKS.json
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same batch
+
+``--impl reference`` times the CPU oracle instead (the only reference arm:
+the pages ship no code).  For N > 1 GPUs each rank runs an independent
+replica (no collective on the data path); value sums the ranks' tokens over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid-batch tokens/s; decode tok/s piggybacked vs decode-only; % of TC/HBM roofline"
+WORKLOAD = "llama13b-hybrid-c256@768-d18@1024"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------- clocks
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [t.strip() for t in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except OSError:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- distributed
+
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, target_s: float):
+    """Time the oracle on the first rows of the chunk plus the first decodes.
+
+    Rows are chosen so the sample respects causality (chunk rows 0..s-1) and
+    grows until about target_s seconds of wall time.  Returns
+    (rows_per_s, rows, seconds, threads).
+    """
+    from oracle import oracle as orc
+    from chunked_prefill_hybrid_gb300 import synth
+    threads = orc.max_threads()
+    pools = orc.Pool(w.num_blocks, w.dims.n_kv_heads, w.dims.head_dim)
+    for layer, s, k, v in w.prefix:
+        if layer == 0:
+            pools.write(s.block_table, 0, synth.bf16_to_f32(k).astype(np.float64),
+                        synth.bf16_to_f32(v).astype(np.float64))
+    x = synth.bf16_to_f32(w.x).astype(np.float64)
+    T, C = w.T, w.batch.chunk_len
+
+    def run(n_chunk, n_dec):
+        rows = np.zeros(T, bool)
+        rows[:n_chunk] = True
+        rows[C:C + n_dec] = True
+        t0 = time.perf_counter()
+        orc.layer_forward(w.dims, w.weights[0], w.batch, x, pools, mirror=True, rows=rows)
+        return time.perf_counter() - t0, int(rows.sum())
+
+    dt, n = run(max(1, threads // 2), max(1, threads // 2))
+    per_row = dt / n
+    want = int(min(T, max(n, target_s / max(per_row, 1e-9))))
+    n_dec = min(w.batch.n_decodes, want // 2)
+    n_chunk = min(C, want - n_dec)
+    dt, n = run(n_chunk, n_dec)
+    return n / dt, n, dt, threads
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores, same workload."""
+    world, rank, local = dist_init(args.gpus)
+    if rank != 0:
+        return 0
+    from chunked_prefill_hybrid_gb300 import workloads
+    from oracle import oracle as orc
+    orc.build()
+    w = workloads.llama13b_hybrid(seed=2)
+    per_step = []
+    sample = None
+    for i in range(args.warmup + args.steps):
+        rps, n, dt, threads = oracle_sample(w, target_s=args.ref_seconds)
+        if i >= args.warmup:
+            per_step.append((rps, n, dt))
+        sample = f"first {n // 2} chunk rows + decode rows ({n} rows of {w.T}), one layer, fp64, mirror mode"
+    value = statistics.median([r for r, _, _ in per_step])
+    ms = statistics.median([dt * 1e3 for _, _, dt in per_step])
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": 1, "T": w.T},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU arm
+
+def time_steps(torch, ctx, fn, steps, world):
+    s = torch.cuda.current_stream()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1)
+
+
+def roofline_for(kind, prof, dims, T, D, ctx_len, pk):
+    """Algorithmic bytes / flops of one launch of `kind` and its bound."""
+    H, F, d = dims.hidden, dims.ffn, dims.head_dim
+    nh, nkv = dims.n_heads, dims.n_kv_heads
+    qkv = (nh + 2 * nkv) * d
+    gemms = {  # (N_out, K, extra bytes written/read besides weights and X)
+        "gemm_qkv": (qkv, H, T * qkv * 2),
+        "gemm_o": (H, nh * d, T * H * 2 * 2),
+        "gemm_gate_up": (2 * F, H, T * F * 2),
+        "gemm_down": (H, F, T * H * 2 * 2),
+    }
+    ms, n = prof[kind]
+    per_launch_s = ms / n / 1e3
+    if kind in gemms:
+        N, K, extra = gemms[kind]
+        flops = 2.0 * T * N * K
+        byts = N * K * 2 + T * K * 2 + extra
+    elif kind == "attention":
+        # KV reads of every key attended once per (sequence, kv head), plus q and o
+        kv_keys = sum(ctx_len)
+        byts = kv_keys * 2 * nkv * d * 2 + 2 * T * nh * d * 2
+        flops = 0.0
+    else:
+        byts, flops = 0.0, 0.0
+    t_mem = byts / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    if t_tc > t_mem:
+        ach = flops / per_launch_s / 1e12
+        return {"kernel": kind, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"], "traffic": None, "algorithmic": flops,
+                "per_launch_us": per_launch_s * 1e6, "peak_source": pk["source"] + " (burst)"}
+    ach = byts / per_launch_s / 1e9
+    return {"kernel": kind, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / pk["hbm_gbs"], "traffic": None, "algorithmic": byts,
+            "per_launch_us": per_launch_s * 1e6, "peak_source": pk["source"]}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world, rank, local = dist_init(args.gpus)
+    import torch
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build_library()
+    from chunked_prefill_hybrid_gb300 import native, workloads, synth
+
+    w = workloads.llama13b_hybrid(seed=2 + rank)
+    dims = w.dims
+    ctx = native.Context(workloads.config(w))
+    x = workloads.upload(w, ctx, poison=None)
+    y = torch.empty_like(x)
+    spec = native.Spec(w.batch)
+    T, D, C = w.T, w.batch.n_decodes, w.batch.chunk_len
+
+    # comparison batches over the same pool and weights
+    dec_only = native.Spec(synth.HybridBatch(None, 0, w.batch.decodes))
+    x_dec = x[C:].contiguous()
+    y_dec = torch.empty_like(x_dec)
+    chunk_alone = native.Spec(synth.HybridBatch(w.batch.chunk, C, []))
+    x_chk = x[:C].contiguous()
+    y_chk = torch.empty_like(x_chk)
+
+    def step():
+        ctx.forward(spec, x, y)
+
+    for _ in range(args.warmup):
+        step()
+    ctx.sync()
+
+    # 1) the headline: hybrid batch, inputs resident
+    n0 = ctx.launch_count
+    with Clocks(local) as clk:
+        ms = time_steps(torch, ctx, step, args.steps, world)
+    launches = (ctx.launch_count - n0) // args.steps
+    ctx.sync()
+    clocks = clk.summary()
+    ms = max_over_ranks(world, ms)
+    ms_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # 2) per-kernel timing of the same step (CUDA events around every launch)
+    ctx.profile(True)
+    time_steps(torch, ctx, step, args.steps, world)
+    ctx.sync()
+    prof = ctx.profile_read()
+    ctx.profile(False)
+    total = sum(v[0] for v in prof.values())
+    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / args.steps,
+                   "share": v[0] / total if total else None} for k, v in prof.items()}
+    pk = peaks()
+    dominant = max(prof, key=lambda k: prof[k][0])
+    ctx_lens = [w.batch.chunk.cached + C] + [s.cached + 1 for s in w.batch.decodes]
+    roof = roofline_for(dominant, prof, dims, T, D, ctx_lens, pk)
+    roof_all = {k: roofline_for(k, prof, dims, T, D, ctx_lens, pk) for k in prof if k.startswith(("gemm", "attention"))}
+
+    # 3) decode tokens/s: piggybacked (marginal over the chunk alone) vs decode-only
+    for _ in range(3):
+        ctx.forward(chunk_alone, x_chk, y_chk)
+        ctx.forward(dec_only, x_dec, y_dec)
+    ctx.sync()
+    ms_chunk = time_steps(torch, ctx, lambda: ctx.forward(chunk_alone, x_chk, y_chk), args.steps, world) / args.steps
+    ms_dec = time_steps(torch, ctx, lambda: ctx.forward(dec_only, x_dec, y_dec), args.steps, world) / args.steps
+    marginal_ms = ms_step - ms_chunk
+    decode = {"piggybacked_tok_s": D / (marginal_ms / 1e3) if marginal_ms > 0 else None,
+              "decode_only_tok_s": D / (ms_dec / 1e3),
+              "per_decode_cost_ratio": (ms_dec / D) / (marginal_ms / D) if marginal_ms > 0 else None,
+              "ms_hybrid": ms_step, "ms_chunk_alone": ms_chunk, "ms_decode_only": ms_dec}
+
+    # 4) end to end through the public host-buffer call
+    xh = torch.empty((T, dims.hidden), dtype=torch.int16, pin_memory=True)
+    xh.copy_(x.cpu())
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        ctx.forward_host_ptr(spec, xh.data_ptr(), yh.data_ptr())
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ctx.forward_host_ptr(spec, xh.data_ptr(), yh.data_ptr())
+    e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+    e2e = {"value": world * T * args.steps / e2e_s, "unit": "tokens/s",
+           "h2d_bytes_per_step": T * dims.hidden * 2, "d2h_bytes_per_step": T * dims.hidden * 2}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": 1, "T": T, "chunk": C, "chunk_offset": w.batch.chunk.cached,
+                       "decodes": D, "decode_ctx": 1024, "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (634 MB weights + 399 MB KV read per step)"},
+            "e2e": e2e, "gpu_launches": int(launches * args.steps), "launches_per_step": int(launches),
+            "clocks": clocks, "decode": decode, "roofline": roof, "kernels": kernels, "rooflines": roof_all}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rps, n, dt, threads = oracle_sample(w, target_s=10.0)
+        line["cpu_baseline"] = {"value": rps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} of {w.T} rows (first chunk rows + first decodes), one layer, "
+                                          f"fp64 mirror mode, {dt:.1f} s"}
+    ctx.free()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,34 @@
+// kernels.h -- host-side launchers of the library's CUDA kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace hb {
+
+// RMSNorm: y[t][i] = bf16(x[t][i] * rsqrt(mean_i x[t][i]^2 + eps) * gamma[i]).
+cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, int H, float eps,
+                           cudaStream_t s);
+
+// Reference SIMT GEMM: acc[t][n] = sum_k X[t][k] W[n][k], then the epilogue.
+cudaError_t launch_gemm_simt(const bf16 *X, const bf16 *W, int T, int N, int K, const EpiParams &ep,
+                             cudaStream_t s);
+
+// Straightforward attention: one CTA per (row, head), online softmax.
+cudaError_t launch_attention_simple(const bf16 *q, const bf16 *k_pool, const bf16 *v_pool, const BatchDev &b,
+                                    int n_heads, int n_kv, int head_dim, bf16 *out, cudaStream_t s);
+
+// Scatter / gather of K,V tokens between dense [n][n_kv][d] and the paged pool.
+cudaError_t launch_kv_write(bf16 *k_pool, bf16 *v_pool, const bf16 *k, const bf16 *v, const int *bt, int start_pos,
+                            int n_tokens, int n_kv, int head_dim, int num_blocks, int *err, cudaStream_t s);
+cudaError_t launch_kv_read(const bf16 *k_pool, const bf16 *v_pool, bf16 *k, bf16 *v, const int *bt, int start_pos,
+                           int n_tokens, int n_kv, int head_dim, int num_blocks, int *err, cudaStream_t s);
+cudaError_t launch_fill_u16(uint16_t *p, size_t n, uint16_t bits, cudaStream_t s);
+
+// Weight repacking at load time.
+//   qkv: within every head block of d rows, stored row 2i <- row i, 2i+1 <- row i + d/2.
+//   gate_up: stored row 2j <- gate row j, 2j+1 <- up row j (src rows ffn + j).
+cudaError_t launch_repack_qkv(const bf16 *src, bf16 *dst, int n_rows, int K, int head_dim, cudaStream_t s);
+cudaError_t launch_repack_gate_up(const bf16 *src, bf16 *dst, int ffn, int K, cudaStream_t s);
+cudaError_t launch_bf16_to_f32(const bf16 *src, float *dst, int n, cudaStream_t s);
+
+}  // namespace hb

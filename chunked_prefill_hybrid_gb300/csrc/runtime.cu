@@ -1,0 +1,675 @@
+// runtime.cu -- the C ABI of include/hb.h: context, validation, batch
+// metadata, weight repacking and the per-layer launch sequence.
+//
+// Per layer l of one hybrid batch (rows: chunk first, then decodes -- SARATHI
+// summary, section 3.4 "Decode-Maximal Batching", "How fusion works"):
+//   n1 = RMSNorm(x)                      -> xn
+//   [q|k|v] = n1 W_qkv^T, RoPE, append   -> q scratch, K/V into the paged pool
+//   o = hybrid attention(q, pool)        -> o   (chunk causal over its prefix,
+//                                               decodes over ctx+1 keys)
+//   h = x + o W_o^T                      -> h
+//   n2 = RMSNorm(h)                      -> xn
+//   a = silu(n2 W_g^T) * (n2 W_u^T)      -> act
+//   y = h + a W_d^T                      -> layer output
+// All of it is enqueued on one stream with no host synchronisation.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/hb.h"
+#include "kernels.h"
+#include "runtime_internal.h"
+
+using namespace hb;
+
+namespace {
+
+int fail(std::string *err, int code, const char *fmt, ...)
+{
+    if (err) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        *err = buf;
+    }
+    return code;
+}
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+namespace hb {
+
+int validate_config(const hb_model_config &c, std::string *err)
+{
+    if (c.n_layers <= 0 || c.hidden <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 || c.ffn <= 0)
+        return fail(err, HB_EINVAL, "model dimensions must be positive");
+    if (c.head_dim != 64 && c.head_dim != 128)
+        return fail(err, HB_EINVAL, "head_dim must be 64 or 128 (got %d)", c.head_dim);
+    if (c.hidden != c.n_heads * c.head_dim)
+        return fail(err, HB_EINVAL, "hidden (%d) != n_heads * head_dim (%d)", c.hidden, c.n_heads * c.head_dim);
+    if (c.n_heads % c.n_kv_heads)
+        return fail(err, HB_EINVAL, "n_heads must be a multiple of n_kv_heads");
+    if (c.hidden % 64 || c.ffn % 16)
+        return fail(err, HB_EINVAL, "hidden must be a multiple of 64 and ffn of 16");
+    if (c.block_size != 16)
+        return fail(err, HB_EINVAL, "block_size must be 16 (got %d)", c.block_size);
+    if (c.num_blocks <= 0 || c.max_blocks_per_seq <= 0 || c.max_tokens <= 0 || c.max_decodes < 0 || c.max_pos <= 0)
+        return fail(err, HB_EINVAL, "capacities must be positive");
+    if ((long long)c.max_blocks_per_seq * 16 < c.max_pos)
+        return fail(err, HB_EINVAL, "max_blocks_per_seq * 16 must cover max_pos");
+    if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f))
+        return fail(err, HB_EINVAL, "rms_eps must be >= 0 and rope_theta > 0");
+    return HB_OK;
+}
+
+// Validation and row metadata of one batch (host only, no GPU).
+int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::string *err)
+{
+    if (!s)
+        return fail(err, HB_EINVAL, "spec is NULL");
+    const bool has_chunk = s->chunk_req_id >= 0;
+    if (s->chunk_req_id < -1)
+        return fail(err, HB_EINVAL, "chunk_req_id must be -1 or a request id");
+    if (has_chunk) {
+        if (s->chunk_len <= 0)
+            return fail(err, HB_EINVAL, "chunk_len must be > 0 when there is a chunk");
+        if (s->chunk_offset < 0)
+            return fail(err, HB_EINVAL, "chunk_offset must be >= 0");
+        if (!s->chunk_block_table)
+            return fail(err, HB_EINVAL, "chunk_block_table is NULL");
+    } else if (s->chunk_len != 0) {
+        return fail(err, HB_EINVAL, "chunk_len > 0 needs chunk_req_id >= 0");
+    }
+    if (s->n_decodes < 0)
+        return fail(err, HB_EINVAL, "n_decodes < 0");
+    if (s->n_decodes > c.max_decodes)
+        return fail(err, HB_ERANGE, "n_decodes %d > max_decodes %d", s->n_decodes, c.max_decodes);
+    const int clen = has_chunk ? s->chunk_len : 0;
+    const long long T = (long long)clen + s->n_decodes;
+    if (T <= 0)
+        return fail(err, HB_EINVAL, "empty batch (no chunk and no decodes)");
+    if (T > c.max_tokens)
+        return fail(err, HB_ERANGE, "batch has %lld rows > max_tokens %d", T, c.max_tokens);
+    if (s->n_decodes > 0) {
+        if (!s->decode_req_ids || !s->decode_ctx_lens || !s->decode_block_tables)
+            return fail(err, HB_EINVAL, "decode arrays are NULL");
+        if (s->decode_bt_stride <= 0 || s->decode_bt_stride > c.max_blocks_per_seq)
+            return fail(err, HB_ERANGE, "decode_bt_stride %d outside 1..max_blocks_per_seq", s->decode_bt_stride);
+    }
+    // distinct ids
+    {
+        std::vector<int> ids(s->decode_req_ids, s->decode_req_ids + s->n_decodes);
+        for (int id : ids)
+            if (id < 0)
+                return fail(err, HB_EINVAL, "decode request ids must be >= 0");
+        if (has_chunk)
+            ids.push_back(s->chunk_req_id);
+        std::sort(ids.begin(), ids.end());
+        if (std::adjacent_find(ids.begin(), ids.end()) != ids.end())
+            return fail(err, HB_EINVAL, "duplicate request id in the batch (decode ids and the chunk id must differ)");
+    }
+    p.T = (int)T;
+    p.chunk_len = clen;
+    p.n_seq = (has_chunk ? 1 : 0) + s->n_decodes;
+    p.pos.assign(p.T, 0);
+    p.slot.assign(p.T, 0);
+    p.row_seq.assign(p.T, 0);
+    p.seq_q0.clear();
+    p.seq_nq.clear();
+    p.seq_pos0.clear();
+    p.seq_bt.clear();
+    p.bt.clear();
+    auto add_seq = [&](int q0, int nq, int pos0, const int32_t *bt, int nb_have, const char *what, int idx) -> int {
+        const long long last = (long long)pos0 + nq - 1;
+        if (last >= c.max_pos)
+            return fail(err, HB_ERANGE, "%s %d: position %lld >= max_pos %d", what, idx, last, c.max_pos);
+        const int nb = (int)(last / 16) + 1;
+        if (nb > nb_have)
+            return fail(err, HB_ERANGE, "%s %d: positions up to %lld need %d blocks, table has %d", what, idx, last,
+                        nb, nb_have);
+        if (nb > c.max_blocks_per_seq)
+            return fail(err, HB_ERANGE, "%s %d: needs %d blocks > max_blocks_per_seq %d", what, idx, nb,
+                        c.max_blocks_per_seq);
+        const int bt0 = (int)p.bt.size();
+        for (int b = 0; b < nb; ++b) {
+            if (bt[b] < 0 || bt[b] >= c.num_blocks)
+                return fail(err, HB_ERANGE, "%s %d: block id %d outside [0, %d)", what, idx, bt[b], c.num_blocks);
+            p.bt.push_back(bt[b]);
+        }
+        const int si = (int)p.seq_q0.size();
+        p.seq_q0.push_back(q0);
+        p.seq_nq.push_back(nq);
+        p.seq_pos0.push_back(pos0);
+        p.seq_bt.push_back(bt0);
+        for (int i = 0; i < nq; ++i) {
+            const int ps = pos0 + i;
+            p.pos[q0 + i] = ps;
+            p.slot[q0 + i] = bt[ps / 16] * 16 + ps % 16;
+            p.row_seq[q0 + i] = si;
+        }
+        return HB_OK;
+    };
+    if (has_chunk) {
+        if (s->chunk_n_blocks <= 0)
+            return fail(err, HB_ERANGE, "chunk_n_blocks must be > 0");
+        int rc = add_seq(0, clen, s->chunk_offset, s->chunk_block_table, s->chunk_n_blocks, "chunk", 0);
+        if (rc)
+            return rc;
+    }
+    for (int j = 0; j < s->n_decodes; ++j) {
+        const int ctx = s->decode_ctx_lens[j];
+        if (ctx < 0)
+            return fail(err, HB_EINVAL, "decode %d: ctx %d < 0", j, ctx);
+        int rc = add_seq(clen + j, 1, ctx, s->decode_block_tables + (size_t)j * s->decode_bt_stride,
+                         s->decode_bt_stride, "decode", j);
+        if (rc)
+            return rc;
+    }
+    // no two rows may write the same KV slot
+    {
+        std::vector<int> sl(p.slot);
+        std::sort(sl.begin(), sl.end());
+        if (std::adjacent_find(sl.begin(), sl.end()) != sl.end())
+            return fail(err, HB_EINVAL, "two rows of the batch map to the same KV slot (block tables overlap)");
+    }
+    return HB_OK;
+}
+
+}  // namespace hb
+
+// ------------------------------------------------------------------ context
+
+#define CK(call)                                                                                     \
+    do {                                                                                             \
+        cudaError_t e_ = (call);                                                                     \
+        if (e_ != cudaSuccess)                                                                       \
+            return ctx->set_error(HB_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));         \
+    } while (0)
+
+int hb_ctx::set_error(int code, const char *fmt, ...)
+{
+    char buf[768];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    last_error = buf;
+    return code;
+}
+
+static int ctx_alloc(hb_ctx *ctx, void **p, size_t bytes)
+{
+    if (bytes == 0)
+        bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return ctx->set_error(HB_ENOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+    }
+    ctx->allocations.push_back(*p);
+    return HB_OK;
+}
+
+void hb_ctx::prof_launch_begin(int kind)
+{
+    n_launches++;
+    if (!prof_on)
+        return;
+    if (prof_used >= prof_events.size()) {
+        cudaEvent_t a, b;
+        cudaEventCreate(&a);
+        cudaEventCreate(&b);
+        prof_events.push_back({a, b});
+    }
+    prof_kinds.push_back(kind);
+    cudaEventRecord(prof_events[prof_used].first, stream);
+}
+
+void hb_ctx::prof_launch_end()
+{
+    if (!prof_on)
+        return;
+    cudaEventRecord(prof_events[prof_used].second, stream);
+    prof_used++;
+}
+
+extern "C" int hb_plan(const hb_model_config *cfg, const hb_batch_spec *spec, int32_t *pos, int32_t *slot, char *err,
+                       int err_len)
+{
+    std::string e;
+    if (!cfg) {
+        e = "cfg is NULL";
+    } else {
+        int rc = validate_config(*cfg, &e);
+        if (rc == HB_OK) {
+            Plan p;
+            rc = plan_batch(*cfg, spec, p, &e);
+            if (rc == HB_OK) {
+                if (pos)
+                    std::copy(p.pos.begin(), p.pos.end(), pos);
+                if (slot)
+                    std::copy(p.slot.begin(), p.slot.end(), slot);
+                return p.T;
+            }
+        }
+        if (err && err_len > 0) {
+            snprintf(err, (size_t)err_len, "%s", e.c_str());
+        }
+        return rc;
+    }
+    if (err && err_len > 0)
+        snprintf(err, (size_t)err_len, "%s", e.c_str());
+    return HB_EINVAL;
+}
+
+extern "C" int hb_init(const hb_model_config *cfg, const hb_layer_weights *weights, void *cuda_stream,
+                       hb_ctx **out)
+{
+    if (!out)
+        return HB_EINVAL;
+    *out = nullptr;
+    if (!cfg)
+        return HB_EINVAL;
+    std::string e;
+    if (validate_config(*cfg, &e) != HB_OK)
+        return HB_EINVAL;
+    hb_ctx *ctx = new hb_ctx();
+    ctx->cfg = *cfg;
+    ctx->stream = (cudaStream_t)cuda_stream;
+    const hb_model_config &c = *cfg;
+    int rc = HB_OK;
+    auto bail = [&](int code) {
+        hb_free(ctx);
+        return code;
+    };
+    if (cudaGetDevice(&ctx->device) != cudaSuccess)
+        return bail(HB_ECUDA);
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, ctx->device) != cudaSuccess)
+        return bail(HB_ECUDA);
+    ctx->num_sms = prop.multiProcessorCount;
+    ctx->cc_major = prop.major;
+    ctx->cc_minor = prop.minor;
+
+    const int d = c.head_dim, H = c.hidden, F = c.ffn;
+    const int qd = c.n_heads * d, kvd = c.n_kv_heads * d;
+    ctx->n_qkv = qd + 2 * kvd;
+    ctx->n_qkv_pad = (int)round_up(ctx->n_qkv, 128);
+    ctx->n_gu = 2 * F;
+    ctx->n_gu_pad = (int)round_up(ctx->n_gu, 128);
+
+    // KV pools: [layer][K|V][num_blocks][n_kv][16][d]
+    ctx->kv_elems_per_pool = (size_t)c.num_blocks * c.n_kv_heads * 16 * d;
+    if ((rc = ctx_alloc(ctx, (void **)&ctx->kv, ctx->kv_elems_per_pool * 2 * c.n_layers * sizeof(bf16))))
+        return bail(rc);
+
+    ctx->layers.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        LayerDev &L = ctx->layers[l];
+        if ((rc = ctx_alloc(ctx, (void **)&L.w_qkv, (size_t)ctx->n_qkv_pad * H * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.w_o, (size_t)H * qd * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.w_gu, (size_t)ctx->n_gu_pad * H * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.w_d, (size_t)H * F * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.g1, (size_t)H * sizeof(float))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.g2, (size_t)H * sizeof(float))))
+            return bail(rc);
+        L.k_pool = ctx->kv + ctx->kv_elems_per_pool * (2 * (size_t)l);
+        L.v_pool = ctx->kv + ctx->kv_elems_per_pool * (2 * (size_t)l + 1);
+        if (cudaMemsetAsync(L.w_qkv, 0, (size_t)ctx->n_qkv_pad * H * sizeof(bf16), ctx->stream) != cudaSuccess ||
+            cudaMemsetAsync(L.w_gu, 0, (size_t)ctx->n_gu_pad * H * sizeof(bf16), ctx->stream) != cudaSuccess)
+            return bail(HB_ECUDA);
+    }
+
+    // RoPE table in fp64 on the host, stored fp32: angle = pos * theta^(-2j/d)
+    {
+        const int half = d / 2;
+        std::vector<float2> tab((size_t)c.max_pos * half);
+        for (int p = 0; p < c.max_pos; ++p)
+            for (int j = 0; j < half; ++j) {
+                const double inv = std::pow((double)c.rope_theta, -2.0 * j / (double)d);
+                const double a = (double)p * inv;
+                tab[(size_t)p * half + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+            }
+        if ((rc = ctx_alloc(ctx, (void **)&ctx->rope, tab.size() * sizeof(float2))))
+            return bail(rc);
+        if (cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+            return bail(HB_ECUDA);
+    }
+
+    const size_t MT = (size_t)c.max_tokens;
+    if ((rc = ctx_alloc(ctx, (void **)&ctx->xn, MT * H * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->q, MT * qd * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->attn_o, MT * qd * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->h, MT * H * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->act, MT * F * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->xa, MT * H * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->xb, MT * H * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->host_in, MT * H * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->host_out, MT * H * sizeof(bf16))) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->err_word, sizeof(int))))
+        return bail(rc);
+    if (cudaMemset(ctx->err_word, 0, sizeof(int)) != cudaSuccess)
+        return bail(HB_ECUDA);
+
+    // metadata: 3 T + 4 n_seq + block tables + attention work list
+    const size_t max_seq = (size_t)c.max_decodes + 1;
+    ctx->meta_cap = 3 * MT + 4 * max_seq + max_seq * c.max_blocks_per_seq + kMetaExtraWords(c);
+    if ((rc = ctx_alloc(ctx, (void **)&ctx->d_meta, ctx->meta_cap * sizeof(int))))
+        return bail(rc);
+    for (int i = 0; i < kMetaRing; ++i) {
+        if (cudaMallocHost((void **)&ctx->h_meta[i], ctx->meta_cap * sizeof(int)) != cudaSuccess) {
+            ctx->h_meta[i] = nullptr;
+            return bail(HB_ENOMEM);
+        }
+        if (cudaEventCreateWithFlags(&ctx->meta_ev[i], cudaEventDisableTiming) != cudaSuccess)
+            return bail(HB_ECUDA);
+    }
+    if ((rc = hb_init_fast_path(ctx)))
+        return bail(rc);
+
+    if (weights) {
+        for (int l = 0; l < c.n_layers; ++l) {
+            if ((rc = hb_load_layer(ctx, l, &weights[l])))
+                return bail(rc);
+        }
+    }
+    if (cudaStreamSynchronize(ctx->stream) != cudaSuccess)
+        return bail(HB_ECUDA);
+    *out = ctx;
+    return HB_OK;
+}
+
+extern "C" int hb_load_layer(hb_ctx *ctx, int layer, const hb_layer_weights *w)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    const hb_model_config &c = ctx->cfg;
+    if (layer < 0 || layer >= c.n_layers)
+        return ctx->set_error(HB_ERANGE, "layer %d outside [0, %d)", layer, c.n_layers);
+    if (!w || !w->w_qkv || !w->w_o || !w->w_gate_up || !w->w_down || !w->norm1 || !w->norm2)
+        return ctx->set_error(HB_EINVAL, "layer %d: a weight pointer is NULL", layer);
+    LayerDev &L = ctx->layers[layer];
+    const int H = c.hidden, qd = c.n_heads * c.head_dim, F = c.ffn;
+    cudaStream_t s = ctx->stream;
+    ctx->n_launches += 5;
+    CK(launch_repack_qkv((const bf16 *)w->w_qkv, L.w_qkv, ctx->n_qkv, H, c.head_dim, s));
+    CK(cudaMemcpyAsync(L.w_o, w->w_o, (size_t)H * qd * sizeof(bf16), cudaMemcpyDeviceToDevice, s));
+    CK(launch_repack_gate_up((const bf16 *)w->w_gate_up, L.w_gu, F, H, s));
+    CK(cudaMemcpyAsync(L.w_d, w->w_down, (size_t)H * F * sizeof(bf16), cudaMemcpyDeviceToDevice, s));
+    CK(launch_bf16_to_f32((const bf16 *)w->norm1, L.g1, H, s));
+    CK(launch_bf16_to_f32((const bf16 *)w->norm2, L.g2, H, s));
+    L.loaded = true;
+    return HB_OK;
+}
+
+static int kv_io(hb_ctx *ctx, int layer, const int32_t *bt, int n_blocks, int start_pos, int n_tokens, const void *k,
+                 const void *v, bool write)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    const hb_model_config &c = ctx->cfg;
+    if (layer < 0 || layer >= c.n_layers)
+        return ctx->set_error(HB_ERANGE, "layer %d outside [0, %d)", layer, c.n_layers);
+    if (n_tokens < 0 || start_pos < 0)
+        return ctx->set_error(HB_EINVAL, "n_tokens and start_pos must be >= 0");
+    if (n_tokens == 0)
+        return HB_OK;
+    if (!bt || !k || !v)
+        return ctx->set_error(HB_EINVAL, "NULL pointer");
+    const long long last = (long long)start_pos + n_tokens - 1;
+    const int nb = (int)(last / 16) + 1;
+    if (nb > n_blocks || nb > c.max_blocks_per_seq)
+        return ctx->set_error(HB_ERANGE, "positions up to %lld need %d blocks, table has %d", last, nb, n_blocks);
+    for (int b = 0; b < nb; ++b)
+        if (bt[b] < 0 || bt[b] >= c.num_blocks)
+            return ctx->set_error(HB_ERANGE, "block id %d outside [0, %d)", bt[b], c.num_blocks);
+    // stage the table through the metadata ring
+    int *hm = ctx->next_meta_host();
+    if (!hm)
+        return ctx->set_error(HB_ECUDA, "metadata staging wait failed");
+    if ((size_t)nb > ctx->meta_cap)
+        return ctx->set_error(HB_ERANGE, "table too long");
+    std::copy(bt, bt + nb, hm);
+    CK(cudaMemcpyAsync(ctx->d_meta, hm, nb * sizeof(int), cudaMemcpyHostToDevice, ctx->stream));
+    CK(cudaEventRecord(ctx->meta_ev[ctx->meta_i], ctx->stream));
+    LayerDev &L = ctx->layers[layer];
+    ctx->prof_launch_begin(K_KVIO);
+    cudaError_t e;
+    if (write)
+        e = launch_kv_write(L.k_pool, L.v_pool, (const bf16 *)k, (const bf16 *)v, ctx->d_meta, start_pos, n_tokens,
+                            c.n_kv_heads, c.head_dim, c.num_blocks, ctx->err_word, ctx->stream);
+    else
+        e = launch_kv_read(L.k_pool, L.v_pool, (bf16 *)k, (bf16 *)v, ctx->d_meta, start_pos, n_tokens, c.n_kv_heads,
+                           c.head_dim, c.num_blocks, ctx->err_word, ctx->stream);
+    ctx->prof_launch_end();
+    if (e != cudaSuccess)
+        return ctx->set_error(HB_ECUDA, "kv copy launch: %s", cudaGetErrorString(e));
+    return HB_OK;
+}
+
+extern "C" int hb_append_kv(hb_ctx *ctx, int layer, const int32_t *block_table, int n_blocks, int start_pos,
+                            int n_tokens, const void *k, const void *v)
+{
+    return kv_io(ctx, layer, block_table, n_blocks, start_pos, n_tokens, k, v, true);
+}
+
+extern "C" int hb_read_kv(hb_ctx *ctx, int layer, const int32_t *block_table, int n_blocks, int start_pos,
+                          int n_tokens, void *k, void *v)
+{
+    return kv_io(ctx, layer, block_table, n_blocks, start_pos, n_tokens, k, v, false);
+}
+
+extern "C" int hb_fill_kv(hb_ctx *ctx, uint16_t bits)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    ctx->n_launches++;
+    CK(launch_fill_u16((uint16_t *)ctx->kv, ctx->kv_elems_per_pool * 2 * ctx->cfg.n_layers, bits, ctx->stream));
+    return HB_OK;
+}
+
+int *hb_ctx::next_meta_host()
+{
+    meta_i = (meta_i + 1) % kMetaRing;
+    if (meta_used[meta_i] && cudaEventSynchronize(meta_ev[meta_i]) != cudaSuccess)
+        return nullptr;
+    meta_used[meta_i] = true;
+    return h_meta[meta_i];
+}
+
+// Upload the plan; fills `b` with device pointers into d_meta.
+static int upload_plan(hb_ctx *ctx, const Plan &p, BatchDev &b)
+{
+    int *hm = ctx->next_meta_host();
+    if (!hm)
+        return ctx->set_error(HB_ECUDA, "metadata staging wait failed");
+    size_t at = 0;
+    auto put = [&](const std::vector<int> &v) {
+        const size_t o = at;
+        std::copy(v.begin(), v.end(), hm + at);
+        at += v.size();
+        return ctx->d_meta + o;
+    };
+    b.T = p.T;
+    b.n_seq = p.n_seq;
+    b.chunk_len = p.chunk_len;
+    b.pos = put(p.pos);
+    b.slot = put(p.slot);
+    b.row_seq = put(p.row_seq);
+    b.seq_q0 = put(p.seq_q0);
+    b.seq_nq = put(p.seq_nq);
+    b.seq_pos0 = put(p.seq_pos0);
+    b.seq_bt = put(p.seq_bt);
+    b.bt = put(p.bt);
+    int rc = hb_plan_fast_path(ctx, p, hm, at, b);
+    if (rc)
+        return rc;
+    if (at > ctx->meta_cap)
+        return ctx->set_error(HB_ERANGE, "metadata overflow (%zu > %zu words)", at, ctx->meta_cap);
+    CK(cudaMemcpyAsync(ctx->d_meta, hm, at * sizeof(int), cudaMemcpyHostToDevice, ctx->stream));
+    CK(cudaEventRecord(ctx->meta_ev[ctx->meta_i], ctx->stream));
+    return HB_OK;
+}
+
+static int run_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, const void *x_in, void *x_out)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    const hb_model_config &c = ctx->cfg;
+    if (l0 < 0 || l1 > c.n_layers || l0 >= l1)
+        return ctx->set_error(HB_ERANGE, "layer range [%d, %d) invalid", l0, l1);
+    if (!x_in || !x_out)
+        return ctx->set_error(HB_EINVAL, "x_in / x_out is NULL");
+    for (int l = l0; l < l1; ++l)
+        if (!ctx->layers[l].loaded)
+            return ctx->set_error(HB_ESTATE, "layer %d has no weights", l);
+    Plan &p = ctx->plan;
+    std::string e;
+    int rc = plan_batch(c, spec, p, &e);
+    if (rc)
+        return ctx->set_error(rc, "%s", e.c_str());
+    const int T = p.T;
+    const size_t xbytes = (size_t)T * c.hidden * sizeof(bf16);
+    const char *xi = (const char *)x_in;
+    char *xo = (char *)x_out;
+    if (xi < xo + xbytes && xo < xi + xbytes)
+        return ctx->set_error(HB_EINVAL, "x_in and x_out overlap");
+    BatchDev b;
+    if ((rc = upload_plan(ctx, p, b)))
+        return rc;
+    const bf16 *x = (const bf16 *)x_in;
+    for (int l = l0; l < l1; ++l) {
+        bf16 *y = (l == l1 - 1) ? (bf16 *)x_out : ((l - l0) % 2 == 0 ? ctx->xa : ctx->xb);
+        if ((rc = run_layer(ctx, l, b, x, y)))
+            return rc;
+        x = y;
+    }
+    return HB_OK;
+}
+
+extern "C" int hb_forward(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in, void *x_out)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    return run_layers(ctx, spec, 0, ctx->cfg.n_layers, x_in, x_out);
+}
+
+extern "C" int hb_forward_layers(hb_ctx *ctx, const hb_batch_spec *spec, int layer_begin, int layer_end,
+                                 const void *x_in, void *x_out)
+{
+    return run_layers(ctx, spec, layer_begin, layer_end, x_in, x_out);
+}
+
+extern "C" int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in_host, void *x_out_host)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    if (!x_in_host || !x_out_host)
+        return ctx->set_error(HB_EINVAL, "NULL host buffer");
+    std::string e;
+    Plan tmp;
+    int rc = plan_batch(ctx->cfg, spec, tmp, &e);
+    if (rc)
+        return ctx->set_error(rc, "%s", e.c_str());
+    const size_t bytes = (size_t)tmp.T * ctx->cfg.hidden * sizeof(bf16);
+    CK(cudaMemcpyAsync(ctx->host_in, x_in_host, bytes, cudaMemcpyHostToDevice, ctx->stream));
+    if ((rc = run_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out)))
+        return rc;
+    CK(cudaMemcpyAsync(x_out_host, ctx->host_out, bytes, cudaMemcpyDeviceToHost, ctx->stream));
+    return hb_sync(ctx);
+}
+
+extern "C" int hb_sync(hb_ctx *ctx)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    CK(cudaStreamSynchronize(ctx->stream));
+    int w = 0;
+    CK(cudaMemcpy(&w, ctx->err_word, sizeof(int), cudaMemcpyDeviceToHost));
+    if (w) {
+        CK(cudaMemset(ctx->err_word, 0, sizeof(int)));
+        return ctx->set_error(HB_EDEVICE, "device error word = %d (%s)", w,
+                              w == DERR_MBAR_TIMEOUT  ? "mbarrier wait timed out"
+                              : w == DERR_BAD_SLOT    ? "slot outside the pool"
+                              : w == DERR_TMEM_ALLOC  ? "tensor memory allocation"
+                              : w == DERR_BAD_WORK    ? "work item out of bounds"
+                                                      : "unknown");
+    }
+    return HB_OK;
+}
+
+extern "C" int hb_profile(hb_ctx *ctx, int enable)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    if (enable) {
+        ctx->prof_used = 0;
+        ctx->prof_kinds.clear();
+    }
+    ctx->prof_on = enable != 0;
+    return HB_OK;
+}
+
+extern "C" int hb_profile_read(hb_ctx *ctx, const char **names, double *total_ms, int *launches, int max_kinds)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    double tot[K_NUM_KINDS] = {0};
+    int cnt[K_NUM_KINDS] = {0};
+    for (size_t i = 0; i < ctx->prof_used; ++i) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, ctx->prof_events[i].first, ctx->prof_events[i].second) != cudaSuccess)
+            return ctx->set_error(HB_ECUDA, "cudaEventElapsedTime failed (call hb_sync first)");
+        tot[ctx->prof_kinds[i]] += ms;
+        cnt[ctx->prof_kinds[i]]++;
+    }
+    int n = 0;
+    for (int k = 0; k < K_NUM_KINDS && n < max_kinds; ++k) {
+        if (!cnt[k])
+            continue;
+        if (names)
+            names[n] = kKindNames[k];
+        if (total_ms)
+            total_ms[n] = tot[k];
+        if (launches)
+            launches[n] = cnt[k];
+        ++n;
+    }
+    return n;
+}
+
+extern "C" long long hb_launch_count(hb_ctx *ctx) { return ctx ? ctx->n_launches : -1; }
+
+extern "C" const char *hb_last_error(hb_ctx *ctx) { return ctx ? ctx->last_error.c_str() : "NULL context"; }
+
+extern "C" void hb_free(hb_ctx *ctx)
+{
+    if (!ctx)
+        return;
+    cudaStreamSynchronize(ctx->stream);
+    hb_free_fast_path(ctx);
+    for (void *p : ctx->allocations)
+        cudaFree(p);
+    for (int i = 0; i < kMetaRing; ++i) {
+        if (ctx->h_meta[i])
+            cudaFreeHost(ctx->h_meta[i]);
+        if (ctx->meta_ev[i])
+            cudaEventDestroy(ctx->meta_ev[i]);
+    }
+    for (auto &pr : ctx->prof_events) {
+        cudaEventDestroy(pr.first);
+        cudaEventDestroy(pr.second);
+    }
+    delete ctx;
+}

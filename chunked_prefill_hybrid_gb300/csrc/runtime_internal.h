@@ -1,0 +1,107 @@
+// runtime_internal.h -- the context object behind hb_ctx and the pieces of
+// the runtime shared between runtime.cu (ABI, validation, metadata) and
+// layer.cu (per-layer launch sequence and kernel selection).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "../../include/hb.h"
+#include "common.cuh"
+
+namespace hb {
+
+struct LayerDev {
+    bf16 *w_qkv = nullptr;  // [n_qkv_pad][H], rows permuted within heads (RoPE pairs adjacent)
+    bf16 *w_o = nullptr;    // [H][n_heads d]
+    bf16 *w_gu = nullptr;   // [n_gu_pad][H], gate/up rows interleaved
+    bf16 *w_d = nullptr;    // [H][F]
+    float *g1 = nullptr, *g2 = nullptr;
+    bf16 *k_pool = nullptr, *v_pool = nullptr;  // [num_blocks][n_kv][16][d]
+    bool loaded = false;
+};
+
+// Host-side plan of one batch (rows: chunk first, then decodes).
+struct Plan {
+    int T = 0, n_seq = 0, chunk_len = 0;
+    std::vector<int> pos, slot, row_seq;
+    std::vector<int> seq_q0, seq_nq, seq_pos0, seq_bt, bt;
+};
+
+// Kernel kinds for per-launch timing.
+enum Kind : int {
+    K_RMSNORM = 0,
+    K_GEMM_QKV,
+    K_ATTENTION,
+    K_ATTN_COMBINE,
+    K_GEMM_O,
+    K_GEMM_GATE_UP,
+    K_GEMM_DOWN,
+    K_KVIO,
+    K_GEMM_TEST,
+    K_NUM_KINDS
+};
+static const char *const kKindNames[K_NUM_KINDS] = {"rmsnorm",   "gemm_qkv",       "attention",
+                                                     "attn_combine", "gemm_o",     "gemm_gate_up",
+                                                     "gemm_down", "kv_io",          "gemm_test"};
+
+constexpr int kMetaRing = 4;
+
+struct FastPath;  // tensor-core GEMM and hybrid attention state (layer.cu)
+
+int validate_config(const hb_model_config &c, std::string *err);
+int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::string *err);
+size_t kMetaExtraWords(const hb_model_config &c);
+
+}  // namespace hb
+
+struct hb_ctx {
+    hb_model_config cfg{};
+    cudaStream_t stream = nullptr;
+    int device = 0, num_sms = 0, cc_major = 0, cc_minor = 0;
+    int n_qkv = 0, n_qkv_pad = 0, n_gu = 0, n_gu_pad = 0;
+
+    std::vector<void *> allocations;
+    std::vector<hb::LayerDev> layers;
+    hb::bf16 *kv = nullptr;
+    size_t kv_elems_per_pool = 0;
+    float2 *rope = nullptr;
+    hb::bf16 *xn = nullptr, *q = nullptr, *attn_o = nullptr, *h = nullptr, *act = nullptr;
+    hb::bf16 *xa = nullptr, *xb = nullptr, *host_in = nullptr, *host_out = nullptr;
+    int *err_word = nullptr;
+
+    // batch metadata: pinned staging ring + one device buffer
+    int *d_meta = nullptr;
+    size_t meta_cap = 0;
+    int *h_meta[hb::kMetaRing] = {nullptr};
+    cudaEvent_t meta_ev[hb::kMetaRing] = {nullptr};
+    bool meta_used[hb::kMetaRing] = {false};
+    int meta_i = 0;
+    int *next_meta_host();
+
+    hb::Plan plan;
+    hb::FastPath *fast = nullptr;
+    int gemm_impl = 1;  // 0: SIMT reference, 1: tcgen05
+    int attn_impl = 1;  // 0: simple, 1: hybrid paged attention
+
+    // profiling and launch accounting
+    long long n_launches = 0;
+    bool prof_on = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> prof_events;
+    std::vector<int> prof_kinds;
+    size_t prof_used = 0;
+    void prof_launch_begin(int kind);
+    void prof_launch_end();
+
+    std::string last_error;
+    int set_error(int code, const char *fmt, ...);
+};
+
+// layer.cu
+int hb_init_fast_path(hb_ctx *ctx);
+void hb_free_fast_path(hb_ctx *ctx);
+int hb_plan_fast_path(hb_ctx *ctx, const hb::Plan &p, int *hm, size_t &at, hb::BatchDev &b);
+int run_layer(hb_ctx *ctx, int l, const hb::BatchDev &b, const hb::bf16 *x, hb::bf16 *y);

@@ -1,0 +1,205 @@
+/*
+ * hb.h -- C ABI of the GB300 hybrid-batch forward library (libhb.so).
+ *
+ * One call runs one decode-maximal hybrid batch -- one prefill chunk of a
+ * request at a prefix offset plus D single-token decodes of other requests --
+ * through a LLaMA-style decoder-layer stack on one GPU:
+ *
+ *   "SARATHI: Efficient LLM Inference by Piggybacking Decodes with Chunked
+ *   Prefills" (paper-graph-ui summary), section 3.4:
+ *     - "Chunked-Prefills" / Figure 6: chunk query i at absolute position
+ *       offset+i attends to keys 0..offset+i, the cached prefix plus the
+ *       causal triangle; this equals the full prefill.
+ *     - "Decode-Maximal Batching", "How fusion works": the chunk's rows come
+ *       first, then the decode rows, and every linear op runs once over the
+ *       concatenated rows so the weights are fetched once per batch.
+ *   "Sarathi-Serve Guide: Chunked-Prefills & LLM Serving" (aifetchly):
+ *     - "Deep Dive: Mathematical Formulation and Attention Mechanics": a
+ *       decode with S cached tokens attends S+1 keys (cache plus itself);
+ *       the block-diagonal hybrid mask isolates requests.
+ *     - production checklist, "Paged KV-Cache Page Sizing": 16-token blocks.
+ *   The batch description follows the co-scheduler's iteration batch in the
+ *   same Guide (chunked request, chunk tokens, chunk prefix length, decode
+ *   requests) plus per-request KV block tables.
+ *
+ * Conventions used by every call:
+ *   - Return 0 (HB_OK) or a negative HB_E* code.  On error, nothing was
+ *     enqueued and hb_last_error() describes the cause.  Every argument is
+ *     validated on the host before any launch, so an invalid batch never
+ *     reaches the GPU.
+ *   - "device" pointers are CUDA device memory of the context's GPU; "host"
+ *     pointers are read only during the call.
+ *   - bf16 tensors are raw 16-bit patterns, row-major, densely packed.
+ *   - Work is enqueued on the context's stream and the calls return without
+ *     waiting (stream-ordered); hb_sync() waits and reports device-side
+ *     errors.
+ *   - A context is not thread-safe; use one context per host thread.
+ */
+#ifndef HB_H
+#define HB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+#define HB_OK 0
+#define HB_EINVAL (-1)  /* malformed argument or batch */
+#define HB_ERANGE (-2)  /* block id, position or size outside its bound */
+#define HB_ENOMEM (-3)  /* device or host allocation failed */
+#define HB_ECUDA (-4)   /* a CUDA runtime call failed; hb_last_error has its text */
+#define HB_EDEVICE (-5) /* a kernel reported an error through the device error word */
+#define HB_ESTATE (-6)  /* call not valid in the context's state (e.g. weights missing) */
+
+typedef struct hb_ctx hb_ctx;
+
+/* Model and capacity.  hidden == n_heads * head_dim; n_heads % n_kv_heads == 0;
+ * head_dim in {64, 128}; block_size must be 16. */
+typedef struct {
+    int n_layers;
+    int hidden;
+    int n_heads;
+    int n_kv_heads;
+    int head_dim;
+    int ffn;
+    float rms_eps;      /* RMSNorm epsilon (1e-6 for LLaMA) */
+    float rope_theta;   /* RoPE base (1e4 for LLaMA) */
+    int block_size;     /* tokens per KV block: 16 */
+    int num_blocks;     /* physical KV blocks per layer in the library-owned pool */
+    int max_blocks_per_seq;
+    int max_tokens;     /* upper bound on rows T = chunk_len + n_decodes of one batch */
+    int max_decodes;    /* upper bound on n_decodes */
+    int max_pos;        /* every absolute position is < max_pos */
+} hb_model_config;
+
+/* One layer's weights, device bf16, row-major [out][in]:
+ *   w_qkv     [(n_heads + 2 n_kv_heads) head_dim][hidden]  q rows, k rows, v rows
+ *   w_o       [hidden][n_heads head_dim]
+ *   w_gate_up [2 ffn][hidden]                              gate rows, then up rows
+ *   w_down    [hidden][ffn]
+ *   norm1, norm2 [hidden]                                  RMSNorm gammas
+ * The library copies and repacks them; the caller may free its buffers once
+ * the call's work has completed (hb_sync). */
+typedef struct {
+    const void *w_qkv, *w_o, *w_gate_up, *w_down;
+    const void *norm1, *norm2;
+} hb_layer_weights;
+
+/* One hybrid batch.  All arrays are host memory.
+ *   chunk_req_id      request id of the prefill chunk, or -1 for no chunk
+ *   chunk_offset      tokens of that request already in the KV cache
+ *   chunk_len         prompt tokens prefilled now (0 when there is no chunk)
+ *   chunk_block_table [chunk_n_blocks] physical block ids, logical order;
+ *                     must cover positions 0 .. chunk_offset+chunk_len-1
+ *   n_decodes         decode tokens D
+ *   decode_req_ids    [n_decodes] distinct, none equal to chunk_req_id
+ *   decode_ctx_lens   [n_decodes] tokens already cached; the new token sits
+ *                     at position ctx and attends ctx+1 keys
+ *   decode_block_tables [n_decodes][decode_bt_stride]; row j covers
+ *                     positions 0 .. ctx_j
+ * Row order of x_in / x_out: chunk rows 0..chunk_len-1, then decode rows in
+ * spec order.  Slot of position p: table[p / 16] * 16 + p % 16. */
+typedef struct {
+    int chunk_req_id;
+    int chunk_offset;
+    int chunk_len;
+    const int32_t *chunk_block_table;
+    int chunk_n_blocks;
+    int n_decodes;
+    const int32_t *decode_req_ids;
+    const int32_t *decode_ctx_lens;
+    const int32_t *decode_block_tables;
+    int decode_bt_stride;
+} hb_batch_spec;
+
+/* Create a context on the current CUDA device.
+ * cfg: host.  weights: host array of n_layers entries (device pointers
+ * inside), or NULL to load layers later with hb_load_layer.  cuda_stream: a
+ * cudaStream_t or NULL for the legacy default stream.  *out receives the
+ * context.  Allocates the KV pools (n_layers x 2 x num_blocks x 16 tokens),
+ * repacked weights and all scratch.  Errors: HB_EINVAL (bad dims),
+ * HB_ENOMEM, HB_ECUDA (out is then NULL). */
+int hb_init(const hb_model_config *cfg, const hb_layer_weights *weights, void *cuda_stream, hb_ctx **out);
+
+/* Copy and repack layer `layer`'s weights (see hb_layer_weights). */
+int hb_load_layer(hb_ctx *ctx, int layer, const hb_layer_weights *w);
+
+/* Write n_tokens tokens of K (post-RoPE) and V for positions start_pos ..
+ * start_pos+n_tokens-1 of one request into layer `layer`'s pool.
+ * block_table: host [n_blocks].  k, v: device bf16 [n_tokens][n_kv_heads][head_dim].
+ * Used to load a cached prefix.  Errors: HB_EINVAL, HB_ERANGE. */
+int hb_append_kv(hb_ctx *ctx, int layer, const int32_t *block_table, int n_blocks, int start_pos,
+                 int n_tokens, const void *k, const void *v);
+
+/* Read back K and V of positions start_pos .. start_pos+n_tokens-1 (test
+ * hook; same layout as hb_append_kv, k and v are device outputs). */
+int hb_read_kv(hb_ctx *ctx, int layer, const int32_t *block_table, int n_blocks, int start_pos,
+               int n_tokens, void *k, void *v);
+
+/* Fill every K and V element of every layer's pool with the bf16 pattern
+ * `bits` (test hook: a poison value proves no write lands outside its slot). */
+int hb_fill_kv(hb_ctx *ctx, uint16_t bits);
+
+/* Run the batch through all layers.  x_in, x_out: device bf16 [T][hidden],
+ * T = chunk_len + n_decodes; they may not overlap.  Each layer writes the
+ * batch's new K/V into its pool at the rows' slots, then attends.  The
+ * library does not advance request lengths; the scheduler does. */
+int hb_forward(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in, void *x_out);
+
+/* Same as hb_forward over layers [layer_begin, layer_end) only. */
+int hb_forward_layers(hb_ctx *ctx, const hb_batch_spec *spec, int layer_begin, int layer_end,
+                      const void *x_in, void *x_out);
+
+/* Like hb_forward, but x_in and x_out are HOST bf16 buffers: the call copies
+ * x_in to the device, runs the stack and copies the result back, all on the
+ * context's stream, and waits for it.  Use pinned host memory for speed. */
+int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in_host, void *x_out_host);
+
+/* Wait for the context's stream; returns HB_EDEVICE if a kernel set the
+ * device error word since the last hb_sync (and clears it). */
+int hb_sync(hb_ctx *ctx);
+
+/* Per-kernel timing of the following forwards (CUDA events on the context's
+ * stream around every launch).  enable: 1 starts a fresh window, 0 stops.
+ * hb_profile_read: after hb_sync, fills names[i] (static strings), the summed
+ * milliseconds and launch counts of up to max_kinds kernel kinds; returns the
+ * number of kinds. */
+int hb_profile(hb_ctx *ctx, int enable);
+int hb_profile_read(hb_ctx *ctx, const char **names, double *total_ms, int *launches, int max_kinds);
+
+/* Number of kernel launches enqueued by this context since it was created. */
+long long hb_launch_count(hb_ctx *ctx);
+
+/* Test hook: D[t][n] = sum_k X[t][k] * W[n][k] in fp32, through the same
+ * GEMM kernel the forward uses.  X: device bf16 [T][K]; W: device bf16
+ * [N][K]; D: device fp32 [T][N].  Requires K % 8 == 0. */
+int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int N, int K);
+
+/* Host-only planning of one batch (no GPU, no context needed): validates
+ * spec against cfg exactly as hb_forward does and writes each row's
+ * absolute position and physical KV slot.  pos, slot: host int32 [T] or
+ * NULL; err: host buffer for a message (may be NULL).  Returns T (> 0) or a
+ * negative HB_E* code. */
+int hb_plan(const hb_model_config *cfg, const hb_batch_spec *spec, int32_t *pos, int32_t *slot,
+            char *err, int err_len);
+
+/* Text of the last error on this context (never NULL). */
+const char *hb_last_error(hb_ctx *ctx);
+
+/* Release every allocation of the context (synchronizes its stream first). */
+void hb_free(hb_ctx *ctx);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HB_H */

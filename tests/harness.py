@@ -1,0 +1,61 @@
+"""Shared test helpers: run a workload through the oracle, and compare.
+
+Tolerance (floating point, bf16 layer outputs): mean |gpu - ref| <= 3e-3
+and, elementwise, |gpu - ref| <= max(3e-2, one bf16 ulp of ref), against
+the oracle in bf16-mirror mode.  The ulp allowance only matters where
+|ref| >= 8, where one bf16 step (0.0625) is already larger than 3e-2: there
+the fp32-vs-fp64 accumulation difference can legitimately flip the final
+rounding by one step.  Below 8 the bound is the plain 3e-2.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from chunked_prefill_hybrid_gb300 import synth
+from oracle import oracle as orc
+
+MAX_ABS = 3e-2
+MEAN_ABS = 3e-3
+POISON = 0xFFFF  # bf16 NaN pattern
+
+
+def f64(bits) -> np.ndarray:
+    return synth.bf16_to_f32(bits).astype(np.float64)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def compare(gpu: np.ndarray, ref: np.ndarray, max_abs=MAX_ABS, mean_abs=MEAN_ABS, ulp=True):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    assert np.isfinite(gpu).all(), "non-finite GPU output"
+    err = np.abs(gpu - ref)
+    tol = np.maximum(max_abs, bf16_ulp(ref)) if ulp else np.full_like(ref, max_abs)
+    bad = err > tol
+    stats = {"max_abs": float(err.max()), "mean_abs": float(err.mean()), "n_bad": int(bad.sum()),
+             "max_ref": float(np.abs(ref).max())}
+    ok = (not bad.any()) and stats["mean_abs"] <= mean_abs
+    return ok, stats
+
+
+def oracle_pools(w):
+    pools = [orc.Pool(w.num_blocks, w.dims.n_kv_heads, w.dims.head_dim) for _ in range(w.n_layers)]
+    for layer, s, k, v in w.prefix:
+        pools[layer].write(s.block_table, 0, f64(k), f64(v))
+    return pools
+
+
+def oracle_run(w, rows=None, mirror=True, pools=None):
+    """All layers of the workload through the oracle; returns (y, pools)."""
+    pools = pools if pools is not None else oracle_pools(w)
+    x = f64(w.x)
+    for l in range(w.n_layers):
+        x = orc.layer_forward(w.dims, w.weights[l], w.batch, x, pools[l], mirror=mirror, rows=rows)
+        if rows is not None:
+            x = np.where(np.asarray(rows)[:, None], x, 0.0)
+    return x, pools
