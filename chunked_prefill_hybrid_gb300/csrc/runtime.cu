@@ -649,6 +649,27 @@ extern "C" int hb_profile_read(hb_ctx *ctx, const char **names, double *total_ms
     return n;
 }
 
+extern "C" int hb_debug_read(hb_ctx *ctx, int which, void *dst, int rows)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    const hb_model_config &c = ctx->cfg;
+    if (!dst || rows <= 0 || rows > c.max_tokens)
+        return ctx->set_error(HB_EINVAL, "hb_debug_read: bad arguments");
+    const void *src = nullptr;
+    size_t width = 0;
+    switch (which) {
+    case 0: src = ctx->xn; width = c.hidden; break;
+    case 1: src = ctx->q; width = (size_t)c.n_heads * c.head_dim; break;
+    case 2: src = ctx->attn_o; width = (size_t)c.n_heads * c.head_dim; break;
+    case 3: src = ctx->h; width = c.hidden; break;
+    case 4: src = ctx->act; width = c.ffn; break;
+    default: return ctx->set_error(HB_EINVAL, "hb_debug_read: which %d unknown", which);
+    }
+    CK(cudaMemcpyAsync(dst, src, (size_t)rows * width * sizeof(bf16), cudaMemcpyDeviceToDevice, ctx->stream));
+    return HB_OK;
+}
+
 extern "C" long long hb_launch_count(hb_ctx *ctx) { return ctx ? ctx->n_launches : -1; }
 
 extern "C" const char *hb_last_error(hb_ctx *ctx) { return ctx ? ctx->last_error.c_str() : "NULL context"; }

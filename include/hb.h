@@ -180,6 +180,22 @@ long long hb_launch_count(hb_ctx *ctx);
  * [N][K]; D: device fp32 [T][N].  Requires K % 8 == 0. */
 int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int N, int K);
 
+/* Test hook: choose the kernels later calls use.  gemm_impl 0 = reference
+ * SIMT GEMM, 1 = tcgen05 tensor-core GEMM (default); attn_impl 0 = one CTA
+ * per (row, head), 1 = the paged hybrid-attention kernel (default when
+ * built).  Both settings compute the same function. */
+int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl);
+
+/* Test hook: copy an intermediate of the LAST layer run by the latest
+ * forward into dst (device memory, bf16 rows of the batch):
+ *   which = 0: n1 or n2 (the last RMSNorm output)  [T][hidden]
+ *           1: q after RoPE                        [T][n_heads head_dim]
+ *           2: attention output o                  [T][n_heads head_dim]
+ *           3: h = x + o W_o^T                     [T][hidden]
+ *           4: a = silu(g) * u                     [T][ffn]
+ * Valid after hb_sync.  rows: the batch's T. */
+int hb_debug_read(hb_ctx *ctx, int which, void *dst, int rows);
+
 /* Host-only planning of one batch (no GPU, no context needed): validates
  * spec against cfg exactly as hb_forward does and writes each row's
  * absolute position and physical KV slot.  pos, slot: host int32 [T] or
