@@ -1,0 +1,31 @@
+// attention.h -- host interface of the hybrid paged-attention kernel.
+#pragma once
+
+#include "common.cuh"
+
+namespace hb {
+
+// Keys per decode split; the split count of a decode depends on its context
+// length only, so a decode's result does not depend on the rest of the batch.
+constexpr int ATTN_SPLIT = 256;
+
+struct AttnParams {
+    BatchDev b;
+    const bf16 *q;                   // [T][n_heads][d] after RoPE
+    const bf16 *k_pool, *v_pool;     // [num_blocks][n_kv][16][d]
+    bf16 *out;                       // [T][n_heads][d]
+    int n_heads, n_kv, head_dim;
+    const int *items;                // [n_items][2]
+    int n_items, n_chunk_items;
+    const int *part_off;             // [n_seq] first partial slot of a sequence
+    float *part;                     // split partials (m, l, o[d])
+    int *counters;                   // [n_seq][n_heads], zero between launches
+    int *err;
+};
+
+int attn_smem_bytes(int head_dim);
+int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *items, int *part_off,
+                     int *n_chunk_items);
+cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s);
+
+}  // namespace hb

@@ -1,0 +1,553 @@
+// attention_hybrid.cu -- one launch for the whole hybrid batch's attention.
+//
+// Semantics (Sarathi-Serve Guide, "Deep Dive: Mathematical Formulation and
+// Attention Mechanics"; SARATHI summary, section 3.4 "Chunked-Prefills",
+// Figure 6): a query of a request at absolute position p attends to that
+// request's keys at positions 0..p -- for the prefill chunk, the cached
+// prefix plus the causal triangle inside the chunk; for a decode with S
+// cached tokens, S+1 keys.  Keys of other requests are never visible (the
+// block-diagonal hybrid mask).  softmax(q.k / sqrt(d)) v in fp32.
+//
+// Work items, one CTA each, heavy ones first:
+//   chunk tile  64 query rows of a multi-row sequence x one head.  Flash-
+//               style: Q tile in shared memory, key tiles of 64 gathered from
+//               the paged pool with cp.async (double buffered), S = Q K^T and
+//               O += P V on the tensor cores (mma.sync m16n8k16, bf16 in, fp32
+//               accumulate), online softmax in registers.  P is split into
+//               bf16 hi + lo parts for the PV product so the weights keep
+//               ~16 significant bits.
+//   decode split one head of a single-row sequence over a range of at most
+//               256 keys.  Each 16-token block of K and of V is one contiguous
+//               4 KB run in the pool and is streamed with cp.async.bulk into
+//               an 8-stage shared-memory ring (mbarrier pipeline); 4 warps
+//               each take 4 tokens of a block, warp-shuffle dot products and
+//               an online softmax per warp.  The number of splits depends on
+//               the context length only.  Partial (m, l, o) go to a
+//               workspace; the last split to finish (per-(sequence, head)
+//               arrival counter, no waiting) merges them in split order.
+#include <cuda_runtime.h>
+
+#include "attention.h"
+#include "tc_ptx.cuh"
+
+namespace hb {
+
+using namespace tc;
+
+namespace {
+
+constexpr int CQ = 64;            // chunk tile rows
+constexpr int CK = 64;            // chunk key tile
+constexpr int NSTAGE = 8;         // decode ring depth (16-token blocks)
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr uint64_t WAIT_NS = 2000000000ull;
+
+// byte offset of (row, 16-byte chunk) in a [rows][2 D bytes] tile; the
+// chunk index is XORed with the row so that 8 consecutive rows of one chunk
+// column fall in 8 different bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int chunk)
+{
+    return (uint32_t)(row * (2 * D) + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ------------------------------------------------------------ chunk tile
+
+template <int D>
+__device__ void chunk_tile(const AttnParams &p, int seq, int head, int q0, uint8_t *smem)
+{
+    constexpr int ROWB = 2 * D, NCH = D / 8, KS = D / 16, NT = D / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = head / (p.n_heads / p.n_kv);
+    const int row0 = p.b.seq_q0[seq], nq = p.b.seq_nq[seq], pos0 = p.b.seq_pos0[seq];
+    const int *bt = p.b.bt + p.b.seq_bt[seq];
+    const int qrows = min(CQ, nq - q0);
+    const int last_key = pos0 + q0 + qrows - 1;  // keys 0..last_key
+    const int n_kt = last_key / CK + 1;
+
+    const uint32_t sQ = smem_u32(smem);
+    const uint32_t sK[2] = {sQ + CQ * ROWB, sQ + CQ * ROWB + 2 * CK * ROWB};
+    const uint32_t sV[2] = {sK[0] + CK * ROWB, sK[1] + CK * ROWB};
+
+    // Q tile (rows past the chunk are zero)
+    for (int i = threadIdx.x; i < CQ * NCH; i += blockDim.x) {
+        const int r = i / NCH, ch = i % NCH;
+        const uint32_t dst = sQ + swz<D>(r, ch);
+        if (r < qrows)
+            cp_async16(dst, p.q + ((size_t)(row0 + q0 + r) * p.n_heads + head) * D + ch * 8);
+        else
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0));
+    }
+    auto load_kv = [&](int kt, int buf) {
+        for (int i = threadIdx.x; i < CK * NCH; i += blockDim.x) {
+            const int r = i / NCH, ch = i % NCH;
+            const int kp = kt * CK + r;
+            const uint32_t dk = sK[buf] + swz<D>(r, ch), dv = sV[buf] + swz<D>(r, ch);
+            if (kp <= last_key) {
+                const size_t off = (((size_t)bt[kp >> 4] * p.n_kv + kvh) * 16 + (kp & 15)) * D + ch * 8;
+                cp_async16(dk, p.k_pool + off);
+                cp_async16(dv, p.v_pool + off);
+            } else {
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dk), "r"(0));
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dv), "r"(0));
+            }
+        }
+    };
+    load_kv(0, 0);
+    cp_async_commit();
+
+    const float sl2 = rsqrtf((float)D) * LOG2E;
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    const int wr = warp * 16;                       // this warp's first row in the tile
+    const int qpos[2] = {pos0 + q0 + wr + (lane >> 2), pos0 + q0 + wr + (lane >> 2) + 8};
+    uint32_t qf[KS][4];
+
+    for (int kt = 0; kt < n_kt; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < n_kt)
+            load_kv(kt + 1, buf ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (kt == 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int r = wr + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int ch = ks * 2 + (lane >> 4);
+                ldsm_x4(sQ + swz<D>(r, ch), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+            }
+        }
+        // S = Q K^T (16 rows x 64 keys per warp)
+        float s[8][4];
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+            s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {      // pairs of 8-key n-tiles
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int r = np * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int ch = ks * 2 + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(sK[buf] + swz<D>(r, ch), b0, b1, b2, b3);
+                mma16816(s[np * 2], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+                mma16816(s[np * 2 + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+            }
+        }
+        // mask, online softmax (log2 domain)
+        float mnew[2] = {mrow[0], mrow[1]};
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int kp = kt * CK + n * 8 + (lane & 3) * 2 + (e & 1);
+                const int hr = e >> 1;
+                float v = s[n][e] * sl2;
+                if (kp > qpos[hr])
+                    v = -INFINITY;
+                s[n][e] = v;
+                mnew[hr] = fmaxf(mnew[hr], v);
+            }
+        }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            mnew[hr] = fmaxf(mnew[hr], __shfl_xor_sync(0xffffffffu, mnew[hr], 1));
+            mnew[hr] = fmaxf(mnew[hr], __shfl_xor_sync(0xffffffffu, mnew[hr], 2));
+        }
+        float corr[2], rsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const float mref = (mnew[hr] == -INFINITY) ? 0.f : mnew[hr];
+            corr[hr] = exp2f(mrow[hr] - mref);
+            mrow[hr] = mnew[hr];
+            mnew[hr] = mref;
+        }
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float pv = exp2f(s[n][e] - mnew[e >> 1]);
+                s[n][e] = pv;
+                rsum[e >> 1] += pv;
+            }
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            rsum[hr] += __shfl_xor_sync(0xffffffffu, rsum[hr], 1);
+            rsum[hr] += __shfl_xor_sync(0xffffffffu, rsum[hr], 2);
+            lrow[hr] = lrow[hr] * corr[hr] + rsum[hr];
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            o[n][0] *= corr[0];
+            o[n][1] *= corr[0];
+            o[n][2] *= corr[1];
+            o[n][3] *= corr[1];
+        }
+        // O += P V with P = hi + lo (both bf16)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {       // 16-key steps
+            const float *c0 = s[kk * 2], *c1 = s[kk * 2 + 1];
+            uint32_t ah[4], al[4];
+            {
+                const float x[8] = {c0[0], c0[1], c0[2], c0[3], c1[0], c1[1], c1[2], c1[3]};
+                float hi[8], lo[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    hi[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+                    lo[i] = x[i] - hi[i];
+                }
+                ah[0] = pack_bf16(hi[0], hi[1]);
+                ah[1] = pack_bf16(hi[2], hi[3]);
+                ah[2] = pack_bf16(hi[4], hi[5]);
+                ah[3] = pack_bf16(hi[6], hi[7]);
+                al[0] = pack_bf16(lo[0], lo[1]);
+                al[1] = pack_bf16(lo[2], lo[3]);
+                al[2] = pack_bf16(lo[4], lo[5]);
+                al[3] = pack_bf16(lo[6], lo[7]);
+            }
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {   // pairs of 8-dim n-tiles
+                const int r = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int ch = dp * 2 + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(sV[buf] + swz<D>(r, ch), b0, b1, b2, b3);
+                mma16816(o[dp * 2], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                mma16816(o[dp * 2 + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
+                mma16816(o[dp * 2], al[0], al[1], al[2], al[3], b0, b1);
+                mma16816(o[dp * 2 + 1], al[0], al[1], al[2], al[3], b2, b3);
+            }
+        }
+        __syncthreads();  // buffer `buf` is refilled two iterations later
+    }
+    // normalise and store
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = wr + (lane >> 2) + hr * 8;
+        if (r >= qrows)
+            continue;
+        const float inv = 1.f / lrow[hr];
+        bf16 *orow = p.out + ((size_t)(row0 + q0 + r) * p.n_heads + head) * D;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int c = n * 8 + (lane & 3) * 2;
+            *reinterpret_cast<__nv_bfloat162 *>(orow + c) =
+                __floats2bfloat162_rn(o[n][hr * 2] * inv, o[n][hr * 2 + 1] * inv);
+        }
+    }
+}
+
+// ----------------------------------------------------------- decode split
+
+template <int D>
+__device__ void decode_split(const AttnParams &p, int seq, int head, int split, uint8_t *smem)
+{
+    constexpr int E = D / 32, BLK = 16 * D * 2, STG = 2 * BLK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = head / (p.n_heads / p.n_kv);
+    const int row = p.b.seq_q0[seq];
+    const int nkeys = p.b.seq_pos0[seq] + 1;
+    const int *bt = p.b.bt + p.b.seq_bt[seq];
+    const int k0 = split * ATTN_SPLIT, k1 = min(nkeys, k0 + ATTN_SPLIT);
+    const int n_splits = (nkeys + ATTN_SPLIT - 1) / ATTN_SPLIT;
+    const int b0 = k0 >> 4, nb = ((k1 - 1) >> 4) - b0 + 1;
+
+    uint8_t *ring = smem;  // NSTAGE x (K block + V block)
+    uint64_t *full = (uint64_t *)(smem + NSTAGE * STG);
+    uint64_t *empty = full + NSTAGE;
+    volatile int *flags = (volatile int *)(empty + NSTAGE);  // [0] abort, [1] last
+    float *red = (float *)(flags + 4);                       // [4][2 + D]
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // q for this lane's E dims, pre-scaled into the log2 domain
+    const float sl2 = rsqrtf((float)D) * LOG2E;
+    float qv[E], acc[E];
+    {
+        const bf16 *qr = p.q + ((size_t)row * p.n_heads + head) * D + lane * E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+            qv[i] = bf2f(qr[i]) * sl2;
+            acc[i] = 0.f;
+        }
+    }
+    float m = -INFINITY, l = 0.f;
+
+    // producer: thread 0 keeps up to NSTAGE blocks in flight
+    auto issue = [&](int i) {
+        const int s = i % NSTAGE;
+        const size_t off = (((size_t)bt[b0 + i] * p.n_kv + kvh) * 16) * D;
+        mbar_expect_tx(&full[s], STG);
+        bulk_load(ring + s * STG, p.k_pool + off, BLK, &full[s]);
+        bulk_load(ring + s * STG + BLK, p.v_pool + off, BLK, &full[s]);
+    };
+    if (threadIdx.x == 0)
+        for (int i = 0; i < min(nb, NSTAGE); ++i)
+            issue(i);
+
+    bool ok = true;
+    for (int i = 0; i < nb; ++i) {
+        const int s = i % NSTAGE;
+        if (!mbar_wait(&full[s], (uint32_t)(i / NSTAGE) & 1u, &flags[0], WAIT_NS)) {
+            set_dev_err(p.err, DERR_MBAR_TIMEOUT);
+            flags[0] = 1;
+            ok = false;
+            break;
+        }
+        const bf16 *Kb = reinterpret_cast<const bf16 *>(ring + s * STG);
+        const bf16 *Vb = reinterpret_cast<const bf16 *>(ring + s * STG + BLK);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int tok = warp * 4 + j;
+            const int kp = (b0 + i) * 16 + tok;
+            const bf16 *ke = Kb + tok * D + lane * E;
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                dot += qv[e] * bf2f(ke[e]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            if (kp >= k0 && kp < k1) {
+                const float mn = fmaxf(m, dot);
+                const float corr = exp2f(m - mn);
+                const float pv = exp2f(dot - mn);
+                l = l * corr + pv;
+                const bf16 *ve = Vb + tok * D + lane * E;
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    acc[e] = acc[e] * corr + pv * bf2f(ve[e]);
+                m = mn;
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[s]);
+        if (threadIdx.x == 0 && i + NSTAGE < nb) {
+            if (!mbar_wait(&empty[s], (uint32_t)(i / NSTAGE) & 1u, &flags[0], WAIT_NS)) {
+                set_dev_err(p.err, DERR_MBAR_TIMEOUT);
+                flags[0] = 1;
+                ok = false;
+            } else {
+                issue(i + NSTAGE);
+            }
+        }
+        if (flags[0]) {
+            ok = false;
+            break;
+        }
+    }
+    // merge the 4 warps
+    if (lane == 0) {
+        red[warp * (2 + D) + 0] = m;
+        red[warp * (2 + D) + 1] = l;
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        red[warp * (2 + D) + 2 + lane * E + e] = acc[e];
+    __syncthreads();
+    if (!ok) {
+        // let the copies already issued land before the CTA exits
+        if (threadIdx.x == 0)
+            for (int i = 0; i < min(nb, NSTAGE); ++i)
+                mbar_wait(&full[i], 0, nullptr, WAIT_NS / 4);
+        return;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+        M = fmaxf(M, red[w * (2 + D)]);
+    float L = 0.f, f[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float mw = red[w * (2 + D)];
+        f[w] = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        L += red[w * (2 + D) + 1] * f[w];
+    }
+    // thread t < D owns output dim t
+    float ov = 0.f;
+    if (threadIdx.x < D)
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+            ov += red[w * (2 + D) + 2 + threadIdx.x] * f[w];
+    bf16 *orow = p.out + ((size_t)row * p.n_heads + head) * D;
+    if (n_splits == 1) {
+        if (threadIdx.x < D)
+            orow[threadIdx.x] = f2bf(ov / L);
+        return;
+    }
+    // partial (m, l, o) then the last split merges in split order
+    const size_t slot = ((size_t)(p.part_off[seq] + split) * p.n_heads + head) * (2 + D);
+    if (threadIdx.x < D)
+        p.part[slot + 2 + threadIdx.x] = ov;
+    if (threadIdx.x == 0) {
+        p.part[slot] = M;
+        p.part[slot + 1] = L;
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int old = atomicAdd(&p.counters[seq * p.n_heads + head], 1);
+        flags[1] = (old == n_splits - 1);
+    }
+    __syncthreads();
+    if (!flags[1])
+        return;
+    __threadfence();
+    const size_t base = ((size_t)p.part_off[seq] * p.n_heads + head) * (2 + D);
+    const size_t stride = (size_t)p.n_heads * (2 + D);
+    float Mg = -INFINITY;
+    for (int sp = 0; sp < n_splits; ++sp)
+        Mg = fmaxf(Mg, __ldcg(&p.part[base + sp * stride]));
+    float Lg = 0.f, og = 0.f;
+    for (int sp = 0; sp < n_splits; ++sp) {
+        const float ms = __ldcg(&p.part[base + sp * stride]);
+        const float fs = (ms == -INFINITY) ? 0.f : exp2f(ms - Mg);
+        Lg += __ldcg(&p.part[base + sp * stride + 1]) * fs;
+        if (threadIdx.x < D)
+            og += __ldcg(&p.part[base + sp * stride + 2 + threadIdx.x]) * fs;
+    }
+    if (threadIdx.x < D)
+        orow[threadIdx.x] = f2bf(og / Lg);
+    if (threadIdx.x == 0)
+        p.counters[seq * p.n_heads + head] = 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) k_attention_hybrid(AttnParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int item = blockIdx.x / p.n_heads;
+    const int head = blockIdx.x % p.n_heads;
+    if (item >= p.n_items) {
+        if (threadIdx.x == 0)
+            set_dev_err(p.err, DERR_BAD_WORK);
+        return;
+    }
+    const int seq = p.items[2 * item];
+    const int arg = p.items[2 * item + 1];
+    if (item < p.n_chunk_items)
+        chunk_tile<D>(p, seq, head, arg, smem);
+    else
+        decode_split<D>(p, seq, head, arg, smem);
+}
+
+}  // namespace
+
+int attn_smem_bytes(int D)
+{
+    const int chunk = CQ * 2 * D + 4 * CK * 2 * D;                       // Q + 2 x (K, V)
+    const int dec = NSTAGE * 64 * D + 2 * NSTAGE * 8 + 16 + 4 * (2 + D) * 4;
+    return (chunk > dec ? chunk : dec) + 1024;
+}
+
+// Work list: chunk tiles (64 rows) of every sequence with more than one row,
+// then the splits of every single-row sequence.  items: [n_items][2] = (seq,
+// q0 or split); part_off: [n_seq] first partial slot of each sequence.
+int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *items, int *part_off, int *n_chunk_items)
+{
+    int n = 0;
+    for (int s = 0; s < n_seq; ++s)
+        if (seq_nq[s] > 1)
+            for (int q0 = 0; q0 < seq_nq[s]; q0 += CQ) {
+                items[2 * n] = s;
+                items[2 * n + 1] = q0;
+                ++n;
+            }
+    *n_chunk_items = n;
+    int off = 0;
+    for (int s = 0; s < n_seq; ++s) {
+        part_off[s] = off;
+        if (seq_nq[s] == 1) {
+            const int ns = (seq_pos0[s] + 1 + ATTN_SPLIT - 1) / ATTN_SPLIT;
+            for (int sp = 0; sp < ns; ++sp) {
+                items[2 * n] = s;
+                items[2 * n + 1] = sp;
+                ++n;
+            }
+            off += ns;
+        }
+    }
+    return n;
+}
+
+cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s)
+{
+    if (p.n_items <= 0)
+        return cudaSuccess;
+    const int smem = attn_smem_bytes(p.head_dim);
+    static bool configured[2] = {false, false};
+    if (p.head_dim == 128) {
+        if (!configured[1]) {
+            cudaError_t e =
+                cudaFuncSetAttribute(k_attention_hybrid<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess)
+                return e;
+            configured[1] = true;
+        }
+        k_attention_hybrid<128><<<p.n_items * p.n_heads, 128, smem, s>>>(p);
+    } else if (p.head_dim == 64) {
+        if (!configured[0]) {
+            cudaError_t e =
+                cudaFuncSetAttribute(k_attention_hybrid<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess)
+                return e;
+            configured[0] = true;
+        }
+        k_attention_hybrid<64><<<p.n_items * p.n_heads, 128, smem, s>>>(p);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace hb

@@ -1,30 +1,40 @@
 // gemm_tc.cu -- the fused linear ops of the hybrid batch on the sm_103a
-// tensor cores: acc[t][n] = sum_k X[t][k] W[n][k] for all T = C + D rows of
-// the batch at once, so each weight tile is fetched once and serves the
-// chunk's rows and the piggybacked decode rows together (SARATHI summary,
+// tensor cores: acc[t][n] = sum_k X[t][k] W[n][k] over all T = C + D rows of
+// the batch at once, so each weight tile is fetched from HBM once and serves
+// the chunk's rows and the piggybacked decode rows together (SARATHI summary,
 // section 3.4 "Decode-Maximal Batching", "How fusion works").
 //
-// Orientation ("swap AB"): the MMA's M dimension is 128 weight rows (output
-// features), its N dimension is a tile of tokens, a multiple of 16 up to 256.
-// A hybrid batch of 274 rows then runs as two 144-token tiles (5% padding)
-// instead of three 128-row tiles (29% padding): the tile-quantization effect
-// the pages measure (SARATHI summary, section 3.4, Figure 7) is kept small by
-// sizing the token tile to T.
+// Orientation ("swap AB"): the MMA's M is 128 weight rows (output features)
+// and its N is the batch's tokens, a multiple of 16.  A CTA holds every token
+// of the batch for its weight tile (up to 512 tokens as two MMAs of N <= 256
+// into two TMEM accumulators), so T = 256 + 18 = 274 runs as 2 x 144 columns
+// (5% padding) -- the tile-quantization effect of SARATHI summary section
+// 3.4 / Figure 7 is kept small by sizing the token tile to T rather than
+// to a fixed 128.
 //
-// One CTA computes one 128 x NT output tile over the whole K loop:
-//   warp 0      TMA producer: W tile [128][64] and X tile [NT][64] per stage
-//   warp 1      TMEM allocation; one thread issues tcgen05.mma (M=128, N=NT,
-//               K=16, 4 per stage) and commits stage releases
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane =
-//               one output feature, columns = tokens), fused epilogue
-// Every mbarrier wait is bounded (wall-clock limit); on a timeout the kernel
-// records an error in the device error word, drains, frees TMEM and returns.
+// Weights are stored tiled, [n_tile][k_block][128][64], so every TMA box is
+// one contiguous 16 KB run of HBM and each CTA streams a contiguous range.
+//
+// Work split ("stream-K"): the (weight tile, k-block) units are divided
+// evenly over a persistent grid of one CTA per SM.  A tile whose k-range
+// spans several CTAs is finished by the last of them to arrive (per-tile
+// arrival counter, no waiting): it sums every contributor's fp32 partial in
+// CTA order -- a fixed order, so results do not depend on timing -- and runs
+// the fused epilogue.
+//
+//   warp 0      TMA producer: W box [128][64], X boxes [n_sub][64]
+//   warp 1      TMEM owner; one thread issues tcgen05.mma (K = 16, 4 per
+//               k-block per sub-tile) and commits stage / accumulator barriers
+//   warps 2..5  epilogue: tcgen05.ld (one TMEM lane = one output feature,
+//               columns = tokens), fused epilogue or partial write + fixup
+// Every mbarrier wait is bounded (wall clock); on a timeout the kernel
+// records an error in the device error word, drains and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include "kernels.h"
 #include "gemm_tc.h"
+#include "kernels.h"
 #include "tc_ptx.cuh"
 
 namespace hb {
@@ -34,49 +44,79 @@ using namespace tc;
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 constexpr int TC_THREADS = 192;
+constexpr int TC_W_BYTES = TC_BM * TC_BK * 2;
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;  // 2 s
 
-struct TcSmemLayout {
-    int stages, nt, a_bytes, b_bytes, stage_bytes, bar_off, total;
+struct TcArgs {
+    int T, N, K;
+    int n_mtiles, nkb, n_groups;
+    int tg, nsub, n_sub;
+    int units, grid, stages;
+    uint32_t tmem_cols;
+    int n_acc;          // accumulator buffers (2 when one sub-tile fits twice)
+    float *ws;          // [grid][2][tg][128]
+    int *counters;      // [n_mtiles * n_groups]
 };
 
-__host__ __device__ inline TcSmemLayout tc_layout(int nt, int stages)
+__host__ __device__ inline int tc_stage_bytes(int tg) { return TC_W_BYTES + tg * TC_BK * 2; }
+__host__ __device__ inline int tc_smem_bytes(int tg, int stages) { return stages * tc_stage_bytes(tg) + 256 + 1024; }
+
+__device__ __forceinline__ int unit_owner(long long u, const TcArgs &a)
 {
-    TcSmemLayout L;
-    L.stages = stages;
-    L.nt = nt;
-    L.a_bytes = TC_BM * TC_BK * 2;
-    L.b_bytes = nt * TC_BK * 2;
-    L.stage_bytes = L.a_bytes + L.b_bytes;
-    L.bar_off = stages * L.stage_bytes;
-    L.total = L.bar_off + 256 + 1024;  // barriers + alignment slack
-    return L;
+    return (int)((u * a.grid + a.grid - 1) / a.units);
+}
+__device__ __forceinline__ int unit_begin(int c, const TcArgs &a) { return (int)((long long)c * a.units / a.grid); }
+
+// Fused epilogue of 16 consecutive token columns of one feature row.
+__device__ __forceinline__ void epi_cols(const EpiParams &ep, const TcArgs &a, const float (&v)[16], int t_base,
+                                         int n, bool odd)
+{
+    const int n_even = n & ~1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float pv = __shfl_xor_sync(0xffffffffu, v[j], 1);
+        const int t = t_base + j;
+        // even lanes finish even columns, odd lanes odd columns
+        if (t < a.T && (int)odd == (j & 1) && n_even < a.N) {
+            const float a0 = odd ? pv : v[j];
+            const float a1 = odd ? v[j] : pv;
+            epi_pair(ep, t, n_even, a0, a1);
+        }
+    }
 }
 
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int T, int N, int K,
-              int nt, int stages, uint32_t tmem_cols, EpiParams ep)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
+              EpiParams ep)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const TcSmemLayout L = tc_layout(nt, stages);
-    uint64_t *full = (uint64_t *)(smem + L.bar_off);
-    uint64_t *empty = full + stages;
-    uint64_t *accf = empty + stages;
-    uint64_t *drain = accf + 1;
+    const int S = a.stages;
+    const int stage_bytes = tc_stage_bytes(a.tg);
+    uint64_t *full = (uint64_t *)(smem + (size_t)S * stage_bytes);
+    uint64_t *empty = full + S;
+    uint64_t *accf = empty + S;       // [2]
+    uint64_t *acce = accf + 2;        // [2]
+    uint64_t *drain = acce + 2;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * TC_BM, t0 = blockIdx.y * nt;
-    const int nk = (K + TC_BK - 1) / TC_BK;
+    const int cta = blockIdx.x;
+    const int u0 = unit_begin(cta, a), u1 = unit_begin(cta + 1, a);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accf, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);  // one arrival per epilogue warp
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -84,99 +124,204 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_prefetch_desc(&tmX);
     }
     if (warp == 1)
-        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_alloc(tmem_slot, a.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
-        // ---------------- producer
-        int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % stages;
-            const uint32_t use = (uint32_t)(kb / stages);
-            if (kb >= stages && !mbar_wait(&empty[s], (use & 1u) ^ 1u, abort_flag, TC_WAIT_NS)) {
+        // ------------------------------------------------------ producer
+        const uint32_t bytes = (uint32_t)stage_bytes;
+        int it = 0;
+        bool ok = true;
+        for (int u = u0; u < u1 && ok; ++u, ++it) {
+            const int tile = u / a.nkb, kb = u % a.nkb;
+            const int mt = tile / a.n_groups, g = tile % a.n_groups;
+            const int s = it % S;
+            if (it >= S && !mbar_wait(&empty[s], ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, TC_WAIT_NS)) {
                 set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                 *abort_flag = 1;
+                ok = false;
                 break;
             }
-            uint8_t *sa = smem + (size_t)s * L.stage_bytes;
-            mbar_expect_tx(&full[s], (uint32_t)L.stage_bytes);
-            tma_load_2d(sa, &tmW, &full[s], kb * TC_BK, m0);
-            tma_load_2d(sa + L.a_bytes, &tmX, &full[s], kb * TC_BK, t0);
-            issued = kb + 1;
+            uint8_t *sw = smem + (size_t)s * stage_bytes;
+            mbar_expect_tx(&full[s], bytes);
+            tma_load_2d(sw, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM);
+            for (int sub = 0; sub < a.nsub; ++sub)
+                tma_load_2d(sw + TC_W_BYTES + sub * a.n_sub * TC_BK * 2, &tmX, &full[s], kb * TC_BK,
+                            g * a.tg + sub * a.n_sub);
         }
-        if (*abort_flag) {
-            // let the loads already in flight land before the CTA exits
-            for (int kb = (issued > stages ? issued - stages : 0); kb < issued; ++kb)
-                mbar_wait(&full[kb % stages], (uint32_t)(kb / stages) & 1u, nullptr, TC_WAIT_NS / 4);
+        if (!ok) {
+            for (int k = (it > S ? it - S : 0); k < it; ++k)
+                mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u, nullptr, TC_WAIT_NS / 4);
         }
     } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
-        const uint32_t idesc = idesc_bf16_f32(TC_BM, nt);
+        // ------------------------------------------------------ MMA issuer
+        const uint32_t idesc = idesc_bf16_f32(TC_BM, a.n_sub);
+        int it = 0, seg = 0;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % stages;
-            if (!mbar_wait(&full[s], (uint32_t)(kb / stages) & 1u, abort_flag, TC_WAIT_NS)) {
+        for (int u = u0; u < u1 && ok; ++seg) {
+            const int kb0 = u % a.nkb;
+            const int kb1 = min(a.nkb, kb0 + (u1 - u));
+            const int buf = seg % a.n_acc;
+            const int use = seg / a.n_acc;
+            if (use > 0 && !mbar_wait(&acce[buf], (uint32_t)(use - 1) & 1u, abort_flag, TC_WAIT_NS)) {
                 set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                 *abort_flag = 1;
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(smem + (size_t)s * L.stage_bytes);
-            const uint32_t b_base = a_base + (uint32_t)L.a_bytes;
+            const uint32_t d0 = tmem + (uint32_t)(buf * 256);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % S;
+                if (!mbar_wait(&full[s], (uint32_t)(it / S) & 1u, abort_flag, TC_WAIT_NS)) {
+                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t w_base = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint32_t x_base = w_base + TC_W_BYTES;
+                for (int sub = 0; sub < a.nsub; ++sub) {
 #pragma unroll
-            for (int k = 0; k < TC_BK / 16; ++k) {
-                const uint64_t ad = sdesc_kmajor_sw128(a_base + k * 32);
-                const uint64_t bd = sdesc_kmajor_sw128(b_base + k * 32);
-                mma_bf16(tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < TC_BK / 16; ++k) {
+                        const uint64_t ad = sdesc_kmajor_sw128(w_base + k * 32);
+                        const uint64_t bd = sdesc_kmajor_sw128(x_base + sub * a.n_sub * TC_BK * 2 + k * 32);
+                        mma_bf16(d0 + (uint32_t)(sub * 256), ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&empty[s]);
             }
-            mma_commit(&empty[s]);
+            if (!ok)
+                break;
+            mma_commit(&accf[buf]);
+            u += kb1 - kb0;
         }
-        if (ok) {
-            mma_commit(accf);
-        } else {
+        if (!ok) {
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, TC_WAIT_NS / 4);
         }
     } else if (warp >= 2) {
-        // ---------------- epilogue
+        // ------------------------------------------------------ epilogue
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        if (mbar_wait(accf, 0, abort_flag, TC_WAIT_NS * 4)) {
+        const int row = q * 32 + lane;
+        const bool odd = lane & 1;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        int seg = 0;
+        for (int u = u0; u < u1; ++seg) {
+            const int tile = u / a.nkb, kb0 = u % a.nkb;
+            const int kb1 = min(a.nkb, kb0 + (u1 - u));
+            const int mt = tile / a.n_groups, g = tile % a.n_groups;
+            const int buf = seg % a.n_acc;
+            const int use = seg / a.n_acc;
+            if (!mbar_wait(&accf[buf], (uint32_t)use & 1u, abort_flag, TC_WAIT_NS * 2)) {
+                if (!*abort_flag) {
+                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
             tc_fence_after();
-            const int row = q * 32 + lane;
-            const int n = m0 + row;
-            const int n_even = n & ~1;
-            const bool odd = lane & 1;
-            for (int c = 0; c < nt; c += 16) {
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, r);
-                tmem_ld_wait();
+            const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
+            const int n = mt * TC_BM + row;
+            const bool whole = (kb0 == 0 && kb1 == a.nkb);
+            const int slot = (u == u0) ? 0 : 1;
+            float *ws_mine = a.ws + ((size_t)cta * 2 + slot) * a.tg * TC_BM;
+            for (int sub = 0; sub < a.nsub; ++sub) {
+                for (int c = 0; c < a.n_sub; c += 16) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c), r);
+                    tmem_ld_wait();
+                    const int col = sub * a.n_sub + c;
+                    if (whole) {
+                        float v[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float v = __uint_as_float(r[j]);
-                    const float pv = __shfl_xor_sync(0xffffffffu, v, 1);
-                    const int t = t0 + c + j;
-                    // even lanes take even tokens, odd lanes odd tokens
-                    if (t < T && (int)odd == (j & 1) && n_even < N) {
-                        const float a0 = odd ? pv : v;
-                        const float a1 = odd ? v : pv;
-                        epi_pair(ep, t, n_even, a0, a1);
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = __uint_as_float(r[j]);
+                        epi_cols(ep, a, v, g * a.tg + col, n, odd);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            ws_mine[(size_t)(col + j) * TC_BM + row] = __uint_as_float(r[j]);
                     }
                 }
             }
-        } else if (!*abort_flag) {
-            set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-            *abort_flag = 1;
+            // accumulator buffer free for the MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acce[buf]);
+            if (!whole) {
+                // stream-K fixup: the last contributor to arrive finishes the tile
+                __threadfence();
+                epi_bar();
+                if (warp == 2 && lane == 0) {
+                    const int c_lo = unit_owner((long long)tile * a.nkb, a);
+                    const int c_hi = unit_owner((long long)tile * a.nkb + a.nkb - 1, a);
+                    const int old = atomicAdd(&a.counters[tile], 1);
+                    *last_flag = (old == c_hi - c_lo);
+                }
+                epi_bar();
+                if (*last_flag) {
+                    __threadfence();
+                    const int c_lo = unit_owner((long long)tile * a.nkb, a);
+                    const int c_hi = unit_owner((long long)tile * a.nkb + a.nkb - 1, a);
+                    for (int col0 = 0; col0 < a.tg; col0 += 16) {
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = 0.f;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const int cslot = (unit_begin(c, a) / a.nkb == tile) ? 0 : 1;
+                            const float *p = a.ws + ((size_t)c * 2 + cslot) * a.tg * TC_BM;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                v[j] += __ldcg(&p[(size_t)(col0 + j) * TC_BM + row]);
+                        }
+                        epi_cols(ep, a, v, g * a.tg + col0, n, odd);
+                    }
+                    if (warp == 2 && lane == 0)
+                        a.counters[tile] = 0;
+                }
+                epi_bar();
+            }
+            u += kb1 - kb0;
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, tmem_cols);
+        tmem_dealloc(tmem, a.tmem_cols);
+    }
+}
+
+// Rearrange W [N][K] (rows optionally permuted) into [n_tile][k_block][128][64],
+// zero outside N x K.  mode 0: identity rows; 1: RoPE pair permutation
+// within heads of `a` rows; 2: gate/up interleave with ffn = `a`.
+__global__ void k_tile_weights(const bf16 *__restrict__ src, bf16 *__restrict__ dst, int N, int K, int nkb, int mode,
+                               int a)
+{
+    const int r = blockIdx.x;  // destination row in [0, N_pad)
+    int sr = r;
+    if (r < N) {
+        if (mode == 1) {
+            const int hb = r / a, w = r % a;
+            sr = hb * a + (w >> 1) + (w & 1) * (a >> 1);
+        } else if (mode == 2) {
+            sr = (r >> 1) + (r & 1) * a;
+        }
+    }
+    const int mt = r / TC_BM, rr = r % TC_BM;
+    for (int k = threadIdx.x; k < nkb * TC_BK; k += blockDim.x) {
+        const int kb = k / TC_BK, kk = k % TC_BK;
+        bf16 v = __float2bfloat16_rn(0.f);
+        if (r < N && k < K)
+            v = src[(size_t)sr * K + k];
+        dst[(((size_t)mt * nkb + kb) * TC_BM + rr) * TC_BK + kk] = v;
     }
 }
 
@@ -196,15 +341,15 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2D bf16 K-major map: rows x K elements, row stride K * 2 bytes, box 64 x box_rows.
-bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows)
+static bool encode_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                      uint32_t box_inner, uint32_t box_rows)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -212,49 +357,101 @@ bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int rows, int K, int box_
     return r == CUDA_SUCCESS;
 }
 
-// Token tile: balanced tiles of at most 256 tokens, multiple of 16.
-int tc_token_tile(int T)
+size_t tiled_weight_elems(int N, int K)
 {
-    const int ntiles = (T + 255) / 256;
-    int nt = (T + ntiles - 1) / ntiles;
-    nt = (nt + 15) / 16 * 16;
-    return nt < 16 ? 16 : nt;
+    const size_t npad = (size_t)(N + TC_BM - 1) / TC_BM * TC_BM;
+    const size_t nkb = (size_t)(K + TC_BK - 1) / TC_BK;
+    return npad * nkb * TC_BK;
 }
 
-static uint32_t tmem_cols_for(int nt)
+cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mode, int a, cudaStream_t s)
 {
-    uint32_t c = 32;
-    while (c < (uint32_t)nt)
-        c <<= 1;
-    return c;
+    const int npad = (N + TC_BM - 1) / TC_BM * TC_BM;
+    const int nkb = (K + TC_BK - 1) / TC_BK;
+    k_tile_weights<<<npad, 256, 0, s>>>(src, dst, N, K, nkb, mode, a);
+    return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N_pad, int N, int K,
-                           const EpiParams &ep, cudaStream_t s, int max_smem)
+bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K)
+{
+    const uint64_t npad = (uint64_t)(N + TC_BM - 1) / TC_BM * TC_BM;
+    const uint64_t nkb = (uint64_t)(K + TC_BK - 1) / TC_BK;
+    return encode_2d(m, tiled, TC_BK, npad * nkb, TC_BK * 2, TC_BK, TC_BM);
+}
+
+TcShape tc_shape(int T)
+{
+    TcShape sh;
+    if (T <= 256) {
+        sh.nsub = 1;
+        sh.n_sub = (T + 15) / 16 * 16;
+        sh.n_groups = 1;
+    } else if (T <= 512) {
+        sh.nsub = 2;
+        sh.n_sub = ((T + 1) / 2 + 15) / 16 * 16;
+        sh.n_groups = 1;
+    } else {
+        sh.nsub = 1;
+        sh.n_groups = (T + 255) / 256;
+        sh.n_sub = ((T + sh.n_groups - 1) / sh.n_groups + 15) / 16 * 16;
+    }
+    sh.tg = sh.nsub * sh.n_sub;
+    return sh;
+}
+
+size_t tc_workspace_floats(int num_sms, int max_tokens)
+{
+    const TcShape sh = tc_shape(max_tokens < 512 ? max_tokens : 512);
+    const int tg = sh.tg < 512 ? 512 : sh.tg;
+    return (size_t)num_sms * 2 * tg * TC_BM;
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, int K, const EpiParams &ep,
+                           const TcRuntime &rt, cudaStream_t s)
 {
     if (T <= 0)
         return cudaSuccess;
-    if (K % 8 != 0 || N_pad % TC_BM != 0)
+    if (K % 8 != 0)
         return cudaErrorInvalidValue;
-    const int nt = tc_token_tile(T);
-    CUtensorMap tmX;
-    if (!make_tmap_kmajor(&tmX, X, T, K, nt))
+    const TcShape sh = tc_shape(T);
+    TcArgs a;
+    a.T = T;
+    a.N = N;
+    a.K = K;
+    a.n_mtiles = (N + TC_BM - 1) / TC_BM;
+    a.nkb = (K + TC_BK - 1) / TC_BK;
+    a.n_groups = sh.n_groups;
+    a.tg = sh.tg;
+    a.nsub = sh.nsub;
+    a.n_sub = sh.n_sub;
+    const long long units = (long long)a.n_mtiles * a.n_groups * a.nkb;
+    if (units > (1ll << 30) || (long long)a.n_mtiles * a.n_groups > rt.n_counters)
         return cudaErrorInvalidValue;
-    int stages = 8;
-    while (stages > 2 && tc_layout(nt, stages).total > max_smem)
+    a.units = (int)units;
+    a.grid = (int)(units < rt.num_sms ? units : rt.num_sms);
+    if ((size_t)a.grid * 2 * a.tg * TC_BM > rt.ws_floats)
+        return cudaErrorInvalidValue;
+    a.n_acc = (a.nsub == 1) ? 2 : 1;
+    a.tmem_cols = 512;  // two accumulators at columns 0 and 256
+    a.ws = rt.ws;
+    a.counters = rt.counters;
+    int stages = 10;
+    while (stages > 2 && tc_smem_bytes(a.tg, stages) > rt.max_smem)
         --stages;
-    const TcSmemLayout L = tc_layout(nt, stages);
-    if (L.total > max_smem)
+    if (tc_smem_bytes(a.tg, stages) > rt.max_smem)
         return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    CUtensorMap tmX;
+    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.n_sub))
+        return cudaErrorInvalidValue;
     static int configured = 0;
-    if (configured < L.total) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (configured < rt.max_smem) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, rt.max_smem);
         if (e != cudaSuccess)
             return e;
-        configured = max_smem;
+        configured = rt.max_smem;
     }
-    dim3 grid(N_pad / TC_BM, (T + nt - 1) / nt);
-    k_gemm_tc<<<grid, TC_THREADS, L.total, s>>>(tmW, tmX, T, N, K, nt, stages, tmem_cols_for(nt), ep);
+    k_gemm_tc<<<a.grid, TC_THREADS, tc_smem_bytes(a.tg, stages), s>>>(tmW, tmX, a, ep);
     return cudaGetLastError();
 }
 

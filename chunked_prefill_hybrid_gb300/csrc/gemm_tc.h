@@ -1,4 +1,4 @@
-// gemm_tc.h -- host interface of the tcgen05 GEMM.
+// gemm_tc.h -- host interface of the tcgen05 stream-K GEMM.
 #pragma once
 
 #include <cuda.h>
@@ -7,16 +7,34 @@
 
 namespace hb {
 
-// 2D bf16 tensor map of a row-major [rows][K] matrix, box 64 x box_rows,
-// 128-byte swizzle.  Returns false if the driver call is unavailable/fails.
-bool make_tmap_kmajor(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
+// Token tiling of a batch of T rows: n_groups groups of tg = nsub * n_sub
+// columns (nsub MMAs of N = n_sub per k-block).
+struct TcShape {
+    int nsub, n_sub, tg, n_groups;
+};
+TcShape tc_shape(int T);
 
-// Token tile used for a batch of T rows.
-int tc_token_tile(int T);
+// Device resources the GEMM needs (owned by the context).
+struct TcRuntime {
+    int num_sms = 0, max_smem = 0;
+    float *ws = nullptr;      // stream-K partials
+    size_t ws_floats = 0;
+    int *counters = nullptr;  // per-tile arrival counters, zero between launches
+    int n_counters = 0;
+};
+
+size_t tc_workspace_floats(int num_sms, int max_tokens);
+
+// Weights in the tiled layout [n_tile][k_block][128][64] (zero padded).
+size_t tiled_weight_elems(int N, int K);
+// mode 0: rows as given; 1: RoPE pair permutation within heads of `a` rows;
+// 2: gate/up interleave (gate rows 0..a-1, up rows a..2a-1 of src).
+cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mode, int a, cudaStream_t s);
+bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K);
 
 // acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
-// tmW: map of W [N_pad][K] with a 128-row box; X: device [T][K] bf16.
-cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N_pad, int N, int K,
-                           const EpiParams &ep, cudaStream_t s, int max_smem);
+// tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).
+cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, int K, const EpiParams &ep,
+                           const TcRuntime &rt, cudaStream_t s);
 
 }  // namespace hb

@@ -10,7 +10,8 @@ cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, in
                            cudaStream_t s);
 
 // Reference SIMT GEMM: acc[t][n] = sum_k X[t][k] W[n][k], then the epilogue.
-cudaError_t launch_gemm_simt(const bf16 *X, const bf16 *W, int T, int N, int K, const EpiParams &ep,
+// tiled: W is in the tensor-core layout [n/128][k/64][128][64], else [N][K].
+cudaError_t launch_gemm_simt(const bf16 *X, const bf16 *W, int T, int N, int K, bool tiled, const EpiParams &ep,
                              cudaStream_t s);
 
 // Straightforward attention: one CTA per (row, head), online softmax.
@@ -24,11 +25,6 @@ cudaError_t launch_kv_read(const bf16 *k_pool, const bf16 *v_pool, bf16 *k, bf16
                            int n_tokens, int n_kv, int head_dim, int num_blocks, int *err, cudaStream_t s);
 cudaError_t launch_fill_u16(uint16_t *p, size_t n, uint16_t bits, cudaStream_t s);
 
-// Weight repacking at load time.
-//   qkv: within every head block of d rows, stored row 2i <- row i, 2i+1 <- row i + d/2.
-//   gate_up: stored row 2j <- gate row j, 2j+1 <- up row j (src rows ffn + j).
-cudaError_t launch_repack_qkv(const bf16 *src, bf16 *dst, int n_rows, int K, int head_dim, cudaStream_t s);
-cudaError_t launch_repack_gate_up(const bf16 *src, bf16 *dst, int ffn, int K, cudaStream_t s);
 cudaError_t launch_bf16_to_f32(const bf16 *src, float *dst, int n, cudaStream_t s);
 
 }  // namespace hb

@@ -67,8 +67,18 @@ cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, in
 
 constexpr int SG_BT = 64, SG_BN = 64, SG_BK = 32;
 
+// W element (n, k): row-major [N][K], or the tensor-core tiled layout
+// [n / 128][k / 64][n % 128][k % 64].
+__device__ __forceinline__ size_t w_index(int n, int k, int K, bool tiled)
+{
+    if (!tiled)
+        return (size_t)n * K + k;
+    const int nkb = (K + 63) / 64;
+    return (((size_t)(n >> 7) * nkb + (k >> 6)) * 128 + (n & 127)) * 64 + (k & 63);
+}
+
 __global__ void __launch_bounds__(256) k_gemm_simt(const bf16 *__restrict__ X, const bf16 *__restrict__ W, int T,
-                                                   int N, int K, EpiParams ep)
+                                                   int N, int K, bool tiled, EpiParams ep)
 {
     __shared__ float Xs[SG_BK][SG_BT + 4];
     __shared__ float Ws[SG_BK][SG_BN + 4];
@@ -87,7 +97,7 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const bf16 *__restrict__ X, c
         }
         for (int e = tid; e < SG_BN * SG_BK; e += 256) {
             const int r = e / SG_BK, c = e % SG_BK, n = n0 + r, k = k0 + c;
-            Ws[c][r] = (n < N && k < K) ? bf2f(W[(size_t)n * K + k]) : 0.f;
+            Ws[c][r] = (n < N && k < K) ? bf2f(W[w_index(n, k, K, tiled)]) : 0.f;
         }
         __syncthreads();
 #pragma unroll 8
@@ -120,12 +130,13 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const bf16 *__restrict__ X, c
     }
 }
 
-cudaError_t launch_gemm_simt(const bf16 *X, const bf16 *W, int T, int N, int K, const EpiParams &ep, cudaStream_t s)
+cudaError_t launch_gemm_simt(const bf16 *X, const bf16 *W, int T, int N, int K, bool tiled, const EpiParams &ep,
+                             cudaStream_t s)
 {
     if (T <= 0)
         return cudaSuccess;
     dim3 grid((N + SG_BN - 1) / SG_BN, (T + SG_BT - 1) / SG_BT);
-    k_gemm_simt<<<grid, 256, 0, s>>>(X, W, T, N, K, ep);
+    k_gemm_simt<<<grid, 256, 0, s>>>(X, W, T, N, K, tiled, ep);
     return cudaGetLastError();
 }
 
@@ -285,37 +296,7 @@ cudaError_t launch_fill_u16(uint16_t *p, size_t n, uint16_t bits, cudaStream_t s
     return cudaGetLastError();
 }
 
-// -------------------------------------------------------------- repacking
-
-__global__ void k_repack_rows(const bf16 *__restrict__ src, bf16 *__restrict__ dst, int K, int mode, int a)
-{
-    // one CTA per destination row; mode 0: qkv head permutation (a = d),
-    // mode 1: gate/up interleave (a = ffn)
-    const int r = blockIdx.x;
-    int sr;
-    if (mode == 0) {
-        const int d = a, hb = r / d, w = r % d;
-        sr = hb * d + (w >> 1) + (w & 1) * (d >> 1);
-    } else {
-        sr = (r >> 1) + (r & 1) * a;
-    }
-    const uint4 *s = reinterpret_cast<const uint4 *>(src + (size_t)sr * K);
-    uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)r * K);
-    for (int i = threadIdx.x; i < K / 8; i += blockDim.x)
-        o[i] = s[i];
-}
-
-cudaError_t launch_repack_qkv(const bf16 *src, bf16 *dst, int n_rows, int K, int head_dim, cudaStream_t s)
-{
-    k_repack_rows<<<n_rows, 256, 0, s>>>(src, dst, K, 0, head_dim);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_repack_gate_up(const bf16 *src, bf16 *dst, int ffn, int K, cudaStream_t s)
-{
-    k_repack_rows<<<2 * ffn, 256, 0, s>>>(src, dst, K, 1, ffn);
-    return cudaGetLastError();
-}
+// ------------------------------------------------------------- conversion
 
 __global__ void k_bf16_to_f32(const bf16 *src, float *dst, int n)
 {

@@ -1,8 +1,10 @@
 // layer.cu -- the per-layer launch sequence and kernel selection.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <vector>
 
+#include "attention.h"
 #include "gemm_tc.h"
 #include "kernels.h"
 #include "runtime_internal.h"
@@ -16,15 +18,26 @@ struct LayerMaps {
 };
 
 struct FastPath {
-    int max_smem = 0;
+    TcRuntime rt;
     std::vector<LayerMaps> maps;
+    bf16 *test_w = nullptr;  // tiled copy of the hb_gemm_test operand
+    size_t test_w_elems = 0;
+    // hybrid attention
+    float *attn_part = nullptr;
+    int *attn_counters = nullptr;
+    std::vector<int> items, part_off;
+    const int *d_items = nullptr, *d_part_off = nullptr;
+    int n_items = 0, n_chunk_items = 0;
 };
 
-size_t kMetaExtraWords(const hb_model_config &c)
+static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + 1; }
+static size_t max_splits_per_seq(const hb_model_config &c) { return ((size_t)c.max_pos + ATTN_SPLIT - 1) / ATTN_SPLIT; }
+static size_t max_items(const hb_model_config &c)
 {
-    (void)c;
-    return 0;
+    return ((size_t)c.max_tokens + 63) / 64 + max_seqs(c) * max_splits_per_seq(c);
 }
+
+size_t kMetaExtraWords(const hb_model_config &c) { return 2 * max_items(c) + max_seqs(c); }
 
 }  // namespace hb
 
@@ -32,37 +45,79 @@ int hb_init_fast_path(hb_ctx *ctx)
 {
     FastPath *f = new FastPath();
     ctx->fast = f;
-    if (cudaDeviceGetAttribute(&f->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device) != cudaSuccess)
+    TcRuntime &rt = f->rt;
+    if (cudaDeviceGetAttribute(&rt.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device) != cudaSuccess)
         return ctx->set_error(HB_ECUDA, "cudaDeviceGetAttribute failed");
+    rt.num_sms = ctx->num_sms;
+    rt.ws_floats = tc_workspace_floats(ctx->num_sms, ctx->cfg.max_tokens);
+    rt.n_counters = 8192;
+    if (cudaMalloc((void **)&rt.ws, rt.ws_floats * sizeof(float)) != cudaSuccess ||
+        cudaMalloc((void **)&rt.counters, rt.n_counters * sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return ctx->set_error(HB_ENOMEM, "GEMM workspace allocation failed");
+    }
+    if (cudaMemset(rt.counters, 0, rt.n_counters * sizeof(int)) != cudaSuccess)
+        return ctx->set_error(HB_ECUDA, "cudaMemset failed");
     const hb_model_config &c = ctx->cfg;
+    {
+        const size_t parts = max_seqs(c) * max_splits_per_seq(c) * c.n_heads * (2 + (size_t)c.head_dim);
+        const size_t cnts = max_seqs(c) * c.n_heads;
+        if (cudaMalloc((void **)&f->attn_part, parts * sizeof(float)) != cudaSuccess ||
+            cudaMalloc((void **)&f->attn_counters, cnts * sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return ctx->set_error(HB_ENOMEM, "attention workspace allocation failed");
+        }
+        if (cudaMemset(f->attn_counters, 0, cnts * sizeof(int)) != cudaSuccess)
+            return ctx->set_error(HB_ECUDA, "cudaMemset failed");
+        f->items.resize(2 * max_items(c));
+        f->part_off.resize(max_seqs(c));
+    }
     const int H = c.hidden, qd = c.n_heads * c.head_dim;
     f->maps.resize(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerDev &L = ctx->layers[l];
         LayerMaps &m = f->maps[l];
-        if (!make_tmap_kmajor(&m.qkv, L.w_qkv, ctx->n_qkv_pad, H, 128) ||
-            !make_tmap_kmajor(&m.o, L.w_o, H, qd, 128) || !make_tmap_kmajor(&m.gu, L.w_gu, ctx->n_gu_pad, H, 128) ||
-            !make_tmap_kmajor(&m.d, L.w_d, H, c.ffn, 128))
+        if (!make_tmap_tiled_weights(&m.qkv, L.w_qkv, ctx->n_qkv, H) ||
+            !make_tmap_tiled_weights(&m.o, L.w_o, H, qd) || !make_tmap_tiled_weights(&m.gu, L.w_gu, ctx->n_gu, H) ||
+            !make_tmap_tiled_weights(&m.d, L.w_d, H, c.ffn))
             return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
     }
     ctx->gemm_impl = 1;
-    ctx->attn_impl = 0;
+    ctx->attn_impl = 1;
     return HB_OK;
 }
 
 void hb_free_fast_path(hb_ctx *ctx)
 {
+    if (ctx->fast) {
+        cudaFree(ctx->fast->rt.ws);
+        cudaFree(ctx->fast->rt.counters);
+        cudaFree(ctx->fast->test_w);
+        cudaFree(ctx->fast->attn_part);
+        cudaFree(ctx->fast->attn_counters);
+    }
     delete ctx->fast;
     ctx->fast = nullptr;
 }
 
+// Attention work list of the batch, appended to the metadata upload.
 int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev &b)
 {
-    (void)ctx;
-    (void)p;
-    (void)hm;
-    (void)at;
     (void)b;
+    FastPath *f = ctx->fast;
+    int n_chunk = 0;
+    const int n = attn_build_items(p.seq_nq.data(), p.seq_pos0.data(), p.n_seq, f->items.data(),
+                                   f->part_off.data(), &n_chunk);
+    if ((size_t)n > max_items(ctx->cfg))
+        return ctx->set_error(HB_ERANGE, "attention work list overflow");
+    std::copy(f->items.begin(), f->items.begin() + 2 * n, hm + at);
+    f->d_items = ctx->d_meta + at;
+    at += 2 * (size_t)n;
+    std::copy(f->part_off.begin(), f->part_off.begin() + p.n_seq, hm + at);
+    f->d_part_off = ctx->d_meta + at;
+    at += p.n_seq;
+    f->n_items = n;
+    f->n_chunk_items = n_chunk;
     return HB_OK;
 }
 
@@ -75,12 +130,13 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
             return ctx->set_error(HB_ECUDA, "launch %s failed: %s", kKindNames[kind], cudaGetErrorString(e_)); \
     } while (0)
 
-static cudaError_t gemm(hb_ctx *ctx, const CUtensorMap *tmW, const bf16 *X, const bf16 *W, int T, int N_pad, int N,
-                        int K, const EpiParams &ep)
+// W is in the tiled layout; tmW its tensor map.
+static cudaError_t gemm(hb_ctx *ctx, const CUtensorMap *tmW, const bf16 *X, const bf16 *W, int T, int N, int K,
+                        const EpiParams &ep)
 {
-    if (ctx->gemm_impl == 1 && tmW)
-        return launch_gemm_tc(*tmW, X, T, N_pad, N, K, ep, ctx->stream, ctx->fast->max_smem);
-    return launch_gemm_simt(X, W, T, N, K, ep, ctx->stream);
+    if (ctx->gemm_impl == 1)
+        return launch_gemm_tc(*tmW, X, T, N, K, ep, ctx->fast->rt, ctx->stream);
+    return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
 }
 
 int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
@@ -108,9 +164,31 @@ int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
     ep.v_pool = L.v_pool;
     ep.num_blocks = c.num_blocks;
     ep.err = ctx->err_word;
-    LK(K_GEMM_QKV, gemm(ctx, &M.qkv, ctx->xn, L.w_qkv, T, ctx->n_qkv_pad, ctx->n_qkv, H, ep));
+    LK(K_GEMM_QKV, gemm(ctx, &M.qkv, ctx->xn, L.w_qkv, T, ctx->n_qkv, H, ep));
 
-    LK(K_ATTENTION, launch_attention_simple(ctx->q, L.k_pool, L.v_pool, b, c.n_heads, c.n_kv_heads, d, ctx->attn_o, s));
+    if (ctx->attn_impl == 1) {
+        const FastPath *f = ctx->fast;
+        AttnParams ap;
+        ap.b = b;
+        ap.q = ctx->q;
+        ap.k_pool = L.k_pool;
+        ap.v_pool = L.v_pool;
+        ap.out = ctx->attn_o;
+        ap.n_heads = c.n_heads;
+        ap.n_kv = c.n_kv_heads;
+        ap.head_dim = d;
+        ap.items = f->d_items;
+        ap.n_items = f->n_items;
+        ap.n_chunk_items = f->n_chunk_items;
+        ap.part_off = f->d_part_off;
+        ap.part = f->attn_part;
+        ap.counters = f->attn_counters;
+        ap.err = ctx->err_word;
+        LK(K_ATTENTION, launch_attention_hybrid(ap, s));
+    } else {
+        LK(K_ATTENTION,
+           launch_attention_simple(ctx->q, L.k_pool, L.v_pool, b, c.n_heads, c.n_kv_heads, d, ctx->attn_o, s));
+    }
 
     EpiParams eo{};
     eo.mode = EPI_RESID;
@@ -118,7 +196,7 @@ int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
     eo.N = H;
     eo.resid = x;
     eo.out = ctx->h;
-    LK(K_GEMM_O, gemm(ctx, &M.o, ctx->attn_o, L.w_o, T, H, H, c.n_heads * d, eo));
+    LK(K_GEMM_O, gemm(ctx, &M.o, ctx->attn_o, L.w_o, T, H, c.n_heads * d, eo));
 
     LK(K_RMSNORM, launch_rmsnorm(ctx->h, L.g2, ctx->xn, T, H, c.rms_eps, s));
 
@@ -128,7 +206,7 @@ int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
     eg.N = ctx->n_gu;
     eg.act = ctx->act;
     eg.ffn = c.ffn;
-    LK(K_GEMM_GATE_UP, gemm(ctx, &M.gu, ctx->xn, L.w_gu, T, ctx->n_gu_pad, ctx->n_gu, H, eg));
+    LK(K_GEMM_GATE_UP, gemm(ctx, &M.gu, ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
 
     EpiParams ed{};
     ed.mode = EPI_RESID;
@@ -136,7 +214,7 @@ int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
     ed.N = H;
     ed.resid = ctx->h;
     ed.out = y;
-    LK(K_GEMM_DOWN, gemm(ctx, &M.d, ctx->act, L.w_d, T, H, H, c.ffn, ed));
+    LK(K_GEMM_DOWN, gemm(ctx, &M.d, ctx->act, L.w_d, T, H, c.ffn, ed));
     return HB_OK;
 }
 
@@ -151,12 +229,30 @@ extern "C" int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, 
     ep.T = T;
     ep.N = N;
     ep.d32 = (float *)D;
+    if (ctx->gemm_impl == 0) {
+        LK(K_GEMM_TEST, launch_gemm_simt((const bf16 *)X, (const bf16 *)W, T, N, K, false, ep, ctx->stream));
+        return HB_OK;
+    }
+    // tile the operand into a scratch copy, then run the tensor-core kernel
+    FastPath *f = ctx->fast;
+    const size_t need = tiled_weight_elems(N, K);
+    if (need > f->test_w_elems) {
+        cudaFree(f->test_w);
+        f->test_w = nullptr;
+        f->test_w_elems = 0;
+        if (cudaMalloc((void **)&f->test_w, need * sizeof(bf16)) != cudaSuccess) {
+            cudaGetLastError();
+            return ctx->set_error(HB_ENOMEM, "hb_gemm_test scratch");
+        }
+        f->test_w_elems = need;
+    }
     CUtensorMap tm;
-    const bool have_map = ctx->gemm_impl == 1 && make_tmap_kmajor(&tm, W, N, K, 128);
-    if (ctx->gemm_impl == 1 && !have_map)
+    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K))
         return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed");
-    LK(K_GEMM_TEST, gemm(ctx, have_map ? &tm : nullptr, (const bf16 *)X, (const bf16 *)W, T, (N + 127) / 128 * 128, N,
-                         K, ep));
+    ctx->n_launches++;
+    if (launch_tile_weights((const bf16 *)W, f->test_w, N, K, 0, 0, ctx->stream) != cudaSuccess)
+        return ctx->set_error(HB_ECUDA, "tile launch failed");
+    LK(K_GEMM_TEST, launch_gemm_tc(tm, (const bf16 *)X, T, N, K, ep, f->rt, ctx->stream));
     return HB_OK;
 }
 

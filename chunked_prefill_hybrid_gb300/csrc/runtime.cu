@@ -23,6 +23,7 @@
 #include <vector>
 
 #include "../../include/hb.h"
+#include "gemm_tc.h"
 #include "kernels.h"
 #include "runtime_internal.h"
 
@@ -317,18 +318,15 @@ extern "C" int hb_init(const hb_model_config *cfg, const hb_layer_weights *weigh
     ctx->layers.resize(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
         LayerDev &L = ctx->layers[l];
-        if ((rc = ctx_alloc(ctx, (void **)&L.w_qkv, (size_t)ctx->n_qkv_pad * H * sizeof(bf16))) ||
-            (rc = ctx_alloc(ctx, (void **)&L.w_o, (size_t)H * qd * sizeof(bf16))) ||
-            (rc = ctx_alloc(ctx, (void **)&L.w_gu, (size_t)ctx->n_gu_pad * H * sizeof(bf16))) ||
-            (rc = ctx_alloc(ctx, (void **)&L.w_d, (size_t)H * F * sizeof(bf16))) ||
+        if ((rc = ctx_alloc(ctx, (void **)&L.w_qkv, tiled_weight_elems(ctx->n_qkv, H) * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.w_o, tiled_weight_elems(H, qd) * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.w_gu, tiled_weight_elems(ctx->n_gu, H) * sizeof(bf16))) ||
+            (rc = ctx_alloc(ctx, (void **)&L.w_d, tiled_weight_elems(H, F) * sizeof(bf16))) ||
             (rc = ctx_alloc(ctx, (void **)&L.g1, (size_t)H * sizeof(float))) ||
             (rc = ctx_alloc(ctx, (void **)&L.g2, (size_t)H * sizeof(float))))
             return bail(rc);
         L.k_pool = ctx->kv + ctx->kv_elems_per_pool * (2 * (size_t)l);
         L.v_pool = ctx->kv + ctx->kv_elems_per_pool * (2 * (size_t)l + 1);
-        if (cudaMemsetAsync(L.w_qkv, 0, (size_t)ctx->n_qkv_pad * H * sizeof(bf16), ctx->stream) != cudaSuccess ||
-            cudaMemsetAsync(L.w_gu, 0, (size_t)ctx->n_gu_pad * H * sizeof(bf16), ctx->stream) != cudaSuccess)
-            return bail(HB_ECUDA);
     }
 
     // RoPE table in fp64 on the host, stored fp32: angle = pos * theta^(-2j/d)
@@ -402,11 +400,12 @@ extern "C" int hb_load_layer(hb_ctx *ctx, int layer, const hb_layer_weights *w)
     LayerDev &L = ctx->layers[layer];
     const int H = c.hidden, qd = c.n_heads * c.head_dim, F = c.ffn;
     cudaStream_t s = ctx->stream;
-    ctx->n_launches += 5;
-    CK(launch_repack_qkv((const bf16 *)w->w_qkv, L.w_qkv, ctx->n_qkv, H, c.head_dim, s));
-    CK(cudaMemcpyAsync(L.w_o, w->w_o, (size_t)H * qd * sizeof(bf16), cudaMemcpyDeviceToDevice, s));
-    CK(launch_repack_gate_up((const bf16 *)w->w_gate_up, L.w_gu, F, H, s));
-    CK(cudaMemcpyAsync(L.w_d, w->w_down, (size_t)H * F * sizeof(bf16), cudaMemcpyDeviceToDevice, s));
+    ctx->n_launches += 6;
+    // tensor-core tiled layout; q/k/v rows paired for RoPE, gate/up rows interleaved
+    CK(launch_tile_weights((const bf16 *)w->w_qkv, L.w_qkv, ctx->n_qkv, H, 1, c.head_dim, s));
+    CK(launch_tile_weights((const bf16 *)w->w_o, L.w_o, H, qd, 0, 0, s));
+    CK(launch_tile_weights((const bf16 *)w->w_gate_up, L.w_gu, ctx->n_gu, H, 2, F, s));
+    CK(launch_tile_weights((const bf16 *)w->w_down, L.w_d, H, F, 0, 0, s));
     CK(launch_bf16_to_f32((const bf16 *)w->norm1, L.g1, H, s));
     CK(launch_bf16_to_f32((const bf16 *)w->norm2, L.g2, H, s));
     L.loaded = true;

@@ -15,10 +15,11 @@
 namespace hb {
 
 struct LayerDev {
-    bf16 *w_qkv = nullptr;  // [n_qkv_pad][H], rows permuted within heads (RoPE pairs adjacent)
-    bf16 *w_o = nullptr;    // [H][n_heads d]
-    bf16 *w_gu = nullptr;   // [n_gu_pad][H], gate/up rows interleaved
-    bf16 *w_d = nullptr;    // [H][F]
+    // weights in the tensor-core tiled layout [N/128][K/64][128][64]
+    bf16 *w_qkv = nullptr;  // N = n_qkv, rows permuted within heads (RoPE pairs adjacent)
+    bf16 *w_o = nullptr;    // N = H, K = n_heads d
+    bf16 *w_gu = nullptr;   // N = 2 ffn, gate/up rows interleaved
+    bf16 *w_d = nullptr;    // N = H, K = ffn
     float *g1 = nullptr, *g2 = nullptr;
     bf16 *k_pool = nullptr, *v_pool = nullptr;  // [num_blocks][n_kv][16][d]
     bool loaded = false;

@@ -22,10 +22,12 @@ def _bits(t):
     return t.cpu().numpy().view(np.uint16)
 
 
-def run_gpu(w, ctx=None, max_tokens=None, max_decodes=None, poison=True):
+def run_gpu(w, ctx=None, max_tokens=None, max_decodes=None, poison=True, kernels=None):
     own = ctx is None
     if own:
         ctx = native.Context(workloads.config(w, max_tokens, max_decodes))
+        if kernels is not None:
+            ctx.set_kernels(*kernels)
         x = workloads.upload(w, ctx, poison=harness.POISON if poison else None)
     else:
         x = workloads.to_device(w.x)
@@ -69,10 +71,16 @@ def check_kv(ctx, w, pools, layer=0):
         assert (kb[used] != harness.POISON).all() and (vb[used] != harness.POISON).all()
 
 
-def _tiny(seed, chunk_offset, chunk_len, ctxs, n_layers=1, gamma="ones"):
+# head_dim 128 and grouped-query shapes at a size the oracle finishes quickly
+D128 = synth.ModelDims(hidden=256, n_heads=2, n_kv_heads=2, head_dim=128, ffn=512)
+GQA = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn=384)
+KERNELS = {"tc+hybrid": (1, 1), "tc+simple": (1, 0), "simt+hybrid": (0, 1)}
+
+
+def _tiny(seed, chunk_offset, chunk_len, ctxs, n_layers=1, gamma="ones", dims=synth.TINY):
     lengths = ([chunk_offset + chunk_len] if chunk_offset is not None else []) + [c + 1 for c in ctxs]
     nb = sum(synth.blocks_needed(n) for n in lengths) + 6
-    return workloads.make("tiny", synth.TINY, seed, chunk_offset, chunk_len, ctxs, n_layers=n_layers,
+    return workloads.make("tiny", dims, seed, chunk_offset, chunk_len, ctxs, n_layers=n_layers,
                           num_blocks=nb, max_pos=nb * 16, gamma=gamma)
 
 
@@ -87,6 +95,7 @@ def test_tiny_hybrid_matches_oracle():
     ctx.free()
 
 
+@pytest.mark.parametrize("kern", sorted(KERNELS))
 @pytest.mark.parametrize("case", [
     ("decode_only", None, 0, [0, 1, 15, 16, 17, 200]),
     ("prefill_only_offset0", 0, 100, []),
@@ -94,13 +103,32 @@ def test_tiny_hybrid_matches_oracle():
     ("ragged_chunk", 5, 77, [31, 32, 33]),
     ("many_decodes", 16, 16, list(range(0, 120, 3))),
     ("ctx0_decode_only", None, 0, [0]),
+    ("multi_split_decodes", 3, 20, [255, 256, 257, 511, 700]),
+    ("long_prefix_chunk", 300, 150, [40]),
 ])
-def test_tiny_edge_cases(case):
+def test_tiny_edge_cases(case, kern):
     name, off, ln, ctxs = case
     w = _tiny(11, off, ln, ctxs)
-    ctx, y = run_gpu(w)
+    ctx, y = run_gpu(w, kernels=KERNELS[kern])
     ref, pools = oracle_run(w)
     ok, st = compare(y, ref, ulp=False)
+    assert ok, (name, st)
+    check_kv(ctx, w, pools)
+    ctx.free()
+
+
+@pytest.mark.parametrize("dims", [D128, GQA], ids=["d128", "gqa"])
+@pytest.mark.parametrize("case", [
+    ("hybrid", 200, 130, [0, 63, 64, 255, 256, 300, 1000]),
+    ("prefill_only", 0, 257, []),
+    ("decode_only", None, 0, [5, 511, 512, 513]),
+])
+def test_head_dim_and_gqa_cases(case, dims):
+    name, off, ln, ctxs = case
+    w = _tiny(15, off, ln, ctxs, dims=dims)
+    ctx, y = run_gpu(w)
+    ref, pools = oracle_run(w)
+    ok, st = compare(y, ref)
     assert ok, (name, st)
     check_kv(ctx, w, pools)
     ctx.free()
