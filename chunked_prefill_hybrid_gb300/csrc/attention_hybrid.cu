@@ -279,6 +279,38 @@ __device__ void chunk_tile(const AttnParams &p, int seq, int head, int q0, uint8
 
 // ----------------------------------------------------------- decode split
 
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Lane that holds token t after the reduce-scatter below (and t of a lane).
+__device__ __forceinline__ int rs_lane_of(int t)
+{
+    return (((t >> 3) & 1) << 4) | (((t >> 2) & 1) << 3) | (((t >> 1) & 1) << 2) | ((t & 1) << 1);
+}
+__device__ __forceinline__ int rs_token_of(int lane)
+{
+    return (((lane >> 4) & 1) << 3) | (((lane >> 3) & 1) << 2) | (((lane >> 2) & 1) << 1) | ((lane >> 1) & 1);
+}
+
+// Keys [k0, k1) of split `split` of a sequence with nkeys keys: the splits
+// are near-equal, 16-aligned, and depend on nkeys alone.
+__device__ __forceinline__ void split_range(int nkeys, int split, int &k0, int &k1, int &n_splits)
+{
+    n_splits = (nkeys + ATTN_SPLIT - 1) / ATTN_SPLIT;
+    int len = (nkeys + n_splits - 1) / n_splits;
+    len = (len + 15) & ~15;
+    k0 = split * len;
+    k1 = min(nkeys, k0 + len);
+}
+
+// One warp takes a whole 16-token block: each lane forms partial dot
+// products of its E dims for all 16 tokens, a reduce-scatter across the
+// warp leaves token t's score in two lanes (16 shuffles per block), one
+// online-softmax step per block, and the weights are broadcast back for
+// the V accumulation.  Warp w handles blocks w, w+4, ...; it owns ring
+// stages w and w+4 and refills them itself, so no cross-warp handshake.
 template <int D>
 __device__ void decode_split(const AttnParams &p, int seq, int head, int split, uint8_t *smem)
 {
@@ -288,25 +320,33 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
     const int row = p.b.seq_q0[seq];
     const int nkeys = p.b.seq_pos0[seq] + 1;
     const int *bt = p.b.bt + p.b.seq_bt[seq];
-    const int k0 = split * ATTN_SPLIT, k1 = min(nkeys, k0 + ATTN_SPLIT);
-    const int n_splits = (nkeys + ATTN_SPLIT - 1) / ATTN_SPLIT;
+    int k0, k1, n_splits;
+    split_range(nkeys, split, k0, k1, n_splits);
     const int b0 = k0 >> 4, nb = ((k1 - 1) >> 4) - b0 + 1;
 
     uint8_t *ring = smem;  // NSTAGE x (K block + V block)
     uint64_t *full = (uint64_t *)(smem + NSTAGE * STG);
-    uint64_t *empty = full + NSTAGE;
-    volatile int *flags = (volatile int *)(empty + NSTAGE);  // [0] abort, [1] last
-    float *red = (float *)(flags + 4);                       // [4][2 + D]
+    volatile int *flags = (volatile int *)(full + NSTAGE);  // [0] abort, [1] last
+    float *red = (float *)(flags + 4);                      // [4][2 + D]
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < NSTAGE; ++s)
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 4);
-        }
         flags[0] = 0;
         fence_mbar_init();
     }
     __syncthreads();
+
+    auto issue = [&](int i) {
+        const int s = i % NSTAGE;
+        const size_t off = (((size_t)bt[b0 + i] * p.n_kv + kvh) * 16) * D;
+        mbar_expect_tx(&full[s], STG);
+        bulk_load(ring + s * STG, p.k_pool + off, BLK, &full[s]);
+        bulk_load(ring + s * STG + BLK, p.v_pool + off, BLK, &full[s]);
+    };
+    if (lane == 0)
+        for (int i = warp; i < min(nb, NSTAGE); i += 4)
+            issue(i);
 
     // q for this lane's E dims, pre-scaled into the log2 domain
     const float sl2 = rsqrtf((float)D) * LOG2E;
@@ -320,69 +360,97 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
         }
     }
     float m = -INFINITY, l = 0.f;
-
-    // producer: thread 0 keeps up to NSTAGE blocks in flight
-    auto issue = [&](int i) {
-        const int s = i % NSTAGE;
-        const size_t off = (((size_t)bt[b0 + i] * p.n_kv + kvh) * 16) * D;
-        mbar_expect_tx(&full[s], STG);
-        bulk_load(ring + s * STG, p.k_pool + off, BLK, &full[s]);
-        bulk_load(ring + s * STG + BLK, p.v_pool + off, BLK, &full[s]);
-    };
-    if (threadIdx.x == 0)
-        for (int i = 0; i < min(nb, NSTAGE); ++i)
-            issue(i);
-
+    const int my_tok = rs_token_of(lane);
     bool ok = true;
-    for (int i = 0; i < nb; ++i) {
+    for (int i = warp; i < nb; i += 4) {
         const int s = i % NSTAGE;
         if (!mbar_wait(&full[s], (uint32_t)(i / NSTAGE) & 1u, &flags[0], WAIT_NS)) {
-            set_dev_err(p.err, DERR_MBAR_TIMEOUT);
-            flags[0] = 1;
-            ok = false;
-            break;
-        }
-        const bf16 *Kb = reinterpret_cast<const bf16 *>(ring + s * STG);
-        const bf16 *Vb = reinterpret_cast<const bf16 *>(ring + s * STG + BLK);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int tok = warp * 4 + j;
-            const int kp = (b0 + i) * 16 + tok;
-            const bf16 *ke = Kb + tok * D + lane * E;
-            float dot = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                dot += qv[e] * bf2f(ke[e]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            if (kp >= k0 && kp < k1) {
-                const float mn = fmaxf(m, dot);
-                const float corr = exp2f(m - mn);
-                const float pv = exp2f(dot - mn);
-                l = l * corr + pv;
-                const bf16 *ve = Vb + tok * D + lane * E;
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    acc[e] = acc[e] * corr + pv * bf2f(ve[e]);
-                m = mn;
-            }
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&empty[s]);
-        if (threadIdx.x == 0 && i + NSTAGE < nb) {
-            if (!mbar_wait(&empty[s], (uint32_t)(i / NSTAGE) & 1u, &flags[0], WAIT_NS)) {
+            if (lane == 0) {
                 set_dev_err(p.err, DERR_MBAR_TIMEOUT);
                 flags[0] = 1;
-                ok = false;
-            } else {
-                issue(i + NSTAGE);
             }
-        }
-        if (flags[0]) {
             ok = false;
             break;
+        }
+        const bf16 *Kb = reinterpret_cast<const bf16 *>(ring + s * STG) + lane * E;
+        const bf16 *Vb = reinterpret_cast<const bf16 *>(ring + s * STG + BLK) + lane * E;
+        float v[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            float d0 = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                d0 += qv[e] * bf2f(Kb[t * D + e]);
+            v[t] = d0;
+        }
+        // reduce-scatter: 16 -> 8 -> 4 -> 2 -> 1 values, then pair sum
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool up = lane & 16;
+            const float send = up ? v[j] : v[8 + j];
+            const float keep = up ? v[8 + j] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool up = lane & 8;
+            const float send = up ? v[j] : v[4 + j];
+            const float keep = up ? v[4 + j] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const bool up = lane & 4;
+            const float send = up ? v[j] : v[2 + j];
+            const float keep = up ? v[2 + j] : v[j];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        {
+            const bool up = lane & 2;
+            const float send = up ? v[0] : v[1];
+            const float keep = up ? v[1] : v[0];
+            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        float sc = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+        const int kp = (b0 + i) * 16 + my_tok;
+        if (kp < k0 || kp >= k1)
+            sc = -INFINITY;
+        float mx = sc;
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m, mx);  // finite: every block has a key in range
+        const float corr = exp2f(m - mn);
+        const float pw = exp2f(sc - mn);
+        float ps = (lane & 1) ? 0.f : pw;
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        l = l * corr + ps;
+        m = mn;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            acc[e] *= corr;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const float pt = __shfl_sync(0xffffffffu, pw, rs_lane_of(t));
+            // tokens outside [k0, k1) have weight 0 and may hold anything
+            // (a slot never written): leave them out rather than add 0 * v
+            if (pt > 0.f) {
+#pragma unroll
+                for (int e = 0; e < E; ++e)
+                    acc[e] += pt * bf2f(Vb[t * D + e]);
+            }
+        }
+        // this warp is the only reader of stage s: refill it
+        if (i + NSTAGE < nb) {
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(i + NSTAGE);
+            }
         }
     }
     // merge the 4 warps
@@ -394,11 +462,11 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
     for (int e = 0; e < E; ++e)
         red[warp * (2 + D) + 2 + lane * E + e] = acc[e];
     __syncthreads();
-    if (!ok) {
+    if (!ok || flags[0]) {
         // let the copies already issued land before the CTA exits
-        if (threadIdx.x == 0)
-            for (int i = 0; i < min(nb, NSTAGE); ++i)
-                mbar_wait(&full[i], 0, nullptr, WAIT_NS / 4);
+        if (lane == 0)
+            for (int i = warp; i < nb; i += 4)
+                mbar_wait(&full[i % NSTAGE], (uint32_t)(i / NSTAGE) & 1u, nullptr, WAIT_NS / 8);
         return;
     }
     float M = -INFINITY;
@@ -486,7 +554,7 @@ __global__ void __launch_bounds__(128) k_attention_hybrid(AttnParams p)
 int attn_smem_bytes(int D)
 {
     const int chunk = CQ * 2 * D + 4 * CK * 2 * D;                       // Q + 2 x (K, V)
-    const int dec = NSTAGE * 64 * D + 2 * NSTAGE * 8 + 16 + 4 * (2 + D) * 4;
+    const int dec = NSTAGE * 64 * D + NSTAGE * 8 + 16 + 4 * (2 + D) * 4;
     return (chunk > dec ? chunk : dec) + 1024;
 }
 
