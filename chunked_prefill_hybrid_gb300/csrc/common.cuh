@@ -121,4 +121,104 @@ __device__ __forceinline__ void epi_pair(const EpiParams &p, int t, int n, float
     }
 }
 
+__device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8])
+{
+    uint4 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        h[k] = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+    return u;
+}
+
+// The same epilogue as epi_pair over 16 consecutive stored output features
+// n0..n0+15 (n0 % 16 == 0) of token t, with 16-byte vector memory accesses.
+// For EPI_QKV the 16 stored rows are 8 RoPE pairs: head features i0..i0+7
+// and i0+d/2..i0+d/2+7; for EPI_SWIGLU they are 8 (gate, up) pairs.
+__device__ __forceinline__ void epi_group(const EpiParams &p, int t, int n0, const float (&v)[16])
+{
+    switch (p.mode) {
+    case EPI_F32: {
+        float *d = p.d32 + (size_t)t * p.N + n0;
+        if (n0 + 16 <= p.N && (p.N & 3) == 0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                reinterpret_cast<float4 *>(d)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                if (n0 + k < p.N)
+                    d[k] = v[k];
+        }
+        break;
+    }
+    case EPI_QKV: {
+        const int d = p.head_dim, half = d >> 1;
+        const int hb = n0 / d, i0 = (n0 % d) >> 1;
+        float lo[8], hi[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            lo[k] = v[2 * k];
+            hi[k] = v[2 * k + 1];
+        }
+        if (hb < p.n_heads + p.n_kv) {
+            const float4 *cs = reinterpret_cast<const float4 *>(p.rope + (size_t)p.pos[t] * half + i0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 c = cs[k];  // (cos, sin) of pairs 2k and 2k+1
+                const float x0 = lo[2 * k], x1 = hi[2 * k], y0 = lo[2 * k + 1], y1 = hi[2 * k + 1];
+                lo[2 * k] = x0 * c.x - x1 * c.y;
+                hi[2 * k] = x1 * c.x + x0 * c.y;
+                lo[2 * k + 1] = y0 * c.z - y1 * c.w;
+                hi[2 * k + 1] = y1 * c.z + y0 * c.w;
+            }
+        }
+        bf16 *base;
+        if (hb < p.n_heads) {
+            base = p.q_out + (size_t)t * p.n_heads * d + (size_t)hb * d;
+        } else {
+            const int s = p.slot[t];
+            const int blk = s >> 4, off = s & 15;
+            if (blk < 0 || blk >= p.num_blocks) {
+                set_dev_err(p.err, DERR_BAD_SLOT);
+                return;
+            }
+            const bool is_k = hb < p.n_heads + p.n_kv;
+            const int kvh = is_k ? hb - p.n_heads : hb - p.n_heads - p.n_kv;
+            base = (is_k ? p.k_pool : p.v_pool) + (((size_t)blk * p.n_kv + kvh) * 16 + off) * d;
+        }
+        *reinterpret_cast<uint4 *>(base + i0) = pack8_bf16(lo);
+        *reinterpret_cast<uint4 *>(base + i0 + half) = pack8_bf16(hi);
+        break;
+    }
+    case EPI_RESID: {
+        const size_t o = (size_t)t * p.N + n0;
+        const uint4 r0 = reinterpret_cast<const uint4 *>(p.resid + o)[0];
+        const uint4 r1 = reinterpret_cast<const uint4 *>(p.resid + o)[1];
+        const bf16 *re0 = reinterpret_cast<const bf16 *>(&r0);
+        const bf16 *re1 = reinterpret_cast<const bf16 *>(&r1);
+        float a[8], b[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            a[k] = bf2f(re0[k]) + v[k];
+            b[k] = bf2f(re1[k]) + v[8 + k];
+        }
+        reinterpret_cast<uint4 *>(p.out + o)[0] = pack8_bf16(a);
+        reinterpret_cast<uint4 *>(p.out + o)[1] = pack8_bf16(b);
+        break;
+    }
+    case EPI_SWIGLU: {
+        const int j0 = n0 >> 1;
+        if (j0 < p.ffn) {
+            float a[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                a[k] = silu_f(v[2 * k]) * v[2 * k + 1];
+            *reinterpret_cast<uint4 *>(p.act + (size_t)t * p.ffn + j0) = pack8_bf16(a);
+        }
+        break;
+    }
+    }
+}
+
 }  // namespace hb

@@ -58,8 +58,15 @@ struct TcArgs {
     int *counters;      // [n_mtiles * n_groups]
 };
 
+// Epilogue staging tile: 32 token columns x 128 features, fp32, padded rows.
+constexpr int TC_STG_LD = 132;
+constexpr int TC_STG_BYTES = 32 * TC_STG_LD * 4;
+
 __host__ __device__ inline int tc_stage_bytes(int tg) { return TC_W_BYTES + tg * TC_BK * 2; }
-__host__ __device__ inline int tc_smem_bytes(int tg, int stages) { return stages * tc_stage_bytes(tg) + 256 + 1024; }
+__host__ __device__ inline int tc_smem_bytes(int tg, int stages)
+{
+    return stages * tc_stage_bytes(tg) + 256 + TC_STG_BYTES + 1024;
+}
 
 __device__ __forceinline__ int unit_owner(long long u, const TcArgs &a)
 {
@@ -67,22 +74,9 @@ __device__ __forceinline__ int unit_owner(long long u, const TcArgs &a)
 }
 __device__ __forceinline__ int unit_begin(int c, const TcArgs &a) { return (int)((long long)c * a.units / a.grid); }
 
-// Fused epilogue of 16 consecutive token columns of one feature row.
-__device__ __forceinline__ void epi_cols(const EpiParams &ep, const TcArgs &a, const float (&v)[16], int t_base,
-                                         int n, bool odd)
+__device__ __forceinline__ void prefetch_l2(const void *p)
 {
-    const int n_even = n & ~1;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const float pv = __shfl_xor_sync(0xffffffffu, v[j], 1);
-        const int t = t_base + j;
-        // even lanes finish even columns, odd lanes odd columns
-        if (t < a.T && (int)odd == (j & 1) && n_even < a.N) {
-            const float a0 = odd ? pv : v[j];
-            const float a1 = odd ? v[j] : pv;
-            epi_pair(ep, t, n_even, a0, a1);
-        }
-    }
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -103,6 +97,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
+    float *stg = (float *)(smem + (size_t)S * stage_bytes + 256);  // [32][TC_STG_LD]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -206,9 +201,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp >= 2) {
         // ------------------------------------------------------ epilogue
+        // TMEM (thread = output feature, registers = tokens) is transposed
+        // through shared memory 32 tokens at a time; each thread then owns
+        // (token, 16 consecutive features) items and applies the fused
+        // epilogue with 16-byte vector accesses.
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int et = threadIdx.x - 64;
         const int row = q * 32 + lane;
-        const bool odd = lane & 1;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int seg = 0;
         for (int u = u0; u < u1; ++seg) {
@@ -217,6 +216,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int mt = tile / a.n_groups, g = tile % a.n_groups;
             const int buf = seg % a.n_acc;
             const int use = seg / a.n_acc;
+            const bool whole = (kb0 == 0 && kb1 == a.nkb);
+            if (whole && ep.mode == EPI_RESID) {
+                // bring this tile's residual rows into L2 while the MMAs run
+                for (int i = et; i < a.tg * 2; i += 128) {
+                    const int t = g * a.tg + (i >> 1);
+                    if (t < a.T)
+                        prefetch_l2(ep.resid + (size_t)t * a.N + mt * TC_BM + (i & 1) * 64);
+                }
+            }
             if (!mbar_wait(&accf[buf], (uint32_t)use & 1u, abort_flag, TC_WAIT_NS * 2)) {
                 if (!*abort_flag) {
                     set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
@@ -226,27 +234,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
-            const int n = mt * TC_BM + row;
-            const bool whole = (kb0 == 0 && kb1 == a.nkb);
             const int slot = (u == u0) ? 0 : 1;
             float *ws_mine = a.ws + ((size_t)cta * 2 + slot) * a.tg * TC_BM;
             for (int sub = 0; sub < a.nsub; ++sub) {
-                for (int c = 0; c < a.n_sub; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c), r);
-                    tmem_ld_wait();
-                    const int col = sub * a.n_sub + c;
-                    if (whole) {
-                        float v[16];
+                for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0 + h * 16), r);
+                        tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            v[j] = __uint_as_float(r[j]);
-                        epi_cols(ep, a, v, g * a.tg + col, n, odd);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            ws_mine[(size_t)(col + j) * TC_BM + row] = __uint_as_float(r[j]);
+                            stg[(h * 16 + j) * TC_STG_LD + row] = __uint_as_float(r[j]);
                     }
+                    epi_bar();
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int it = et + k * 128;
+                        const int j = it >> 3, gq = it & 7;
+                        if (c0 + j < a.n_sub) {
+                            const int col = sub * a.n_sub + c0 + j;
+                            const float4 *sp = reinterpret_cast<const float4 *>(stg + j * TC_STG_LD + gq * 16);
+                            float v[16];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 f = sp[e];
+                                v[4 * e] = f.x;
+                                v[4 * e + 1] = f.y;
+                                v[4 * e + 2] = f.z;
+                                v[4 * e + 3] = f.w;
+                            }
+                            if (whole) {
+                                const int t = g * a.tg + col, n0 = mt * TC_BM + gq * 16;
+                                if (t < a.T && n0 < a.N)
+                                    epi_group(ep, t, n0, v);
+                            } else {
+                                float4 *dst = reinterpret_cast<float4 *>(ws_mine + (size_t)col * TC_BM + gq * 16);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                            }
+                        }
+                    }
+                    epi_bar();
                 }
             }
             // accumulator buffer free for the MMA warp
@@ -258,32 +288,40 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // stream-K fixup: the last contributor to arrive finishes the tile
                 __threadfence();
                 epi_bar();
-                if (warp == 2 && lane == 0) {
-                    const int c_lo = unit_owner((long long)tile * a.nkb, a);
-                    const int c_hi = unit_owner((long long)tile * a.nkb + a.nkb - 1, a);
+                const int c_lo = unit_owner((long long)tile * a.nkb, a);
+                const int c_hi = unit_owner((long long)tile * a.nkb + a.nkb - 1, a);
+                if (et == 0) {
                     const int old = atomicAdd(&a.counters[tile], 1);
                     *last_flag = (old == c_hi - c_lo);
                 }
                 epi_bar();
                 if (*last_flag) {
                     __threadfence();
-                    const int c_lo = unit_owner((long long)tile * a.nkb, a);
-                    const int c_hi = unit_owner((long long)tile * a.nkb + a.nkb - 1, a);
-                    for (int col0 = 0; col0 < a.tg; col0 += 16) {
+                    for (int it = et; it < a.tg * 8; it += 128) {
+                        const int col = it >> 3, gq = it & 7;
+                        const int t = g * a.tg + col, n0 = mt * TC_BM + gq * 16;
+                        if (t >= a.T || n0 >= a.N)
+                            continue;
                         float v[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            v[j] = 0.f;
+                        for (int e = 0; e < 16; ++e)
+                            v[e] = 0.f;
                         for (int c = c_lo; c <= c_hi; ++c) {
                             const int cslot = (unit_begin(c, a) / a.nkb == tile) ? 0 : 1;
-                            const float *p = a.ws + ((size_t)c * 2 + cslot) * a.tg * TC_BM;
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                a.ws + (((size_t)c * 2 + cslot) * a.tg + col) * TC_BM + gq * 16);
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                v[j] += __ldcg(&p[(size_t)(col0 + j) * TC_BM + row]);
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 f = __ldcg(src + e);
+                                v[4 * e] += f.x;
+                                v[4 * e + 1] += f.y;
+                                v[4 * e + 2] += f.z;
+                                v[4 * e + 3] += f.w;
+                            }
                         }
-                        epi_cols(ep, a, v, g * a.tg + col0, n, odd);
+                        epi_group(ep, t, n0, v);
                     }
-                    if (warp == 2 && lane == 0)
+                    if (et == 0)
                         a.counters[tile] = 0;
                 }
                 epi_bar();
