@@ -43,7 +43,9 @@ struct BatchDev {
 };
 
 // Epilogue of the fused GEMMs (fp32 accumulators of output pairs).
-enum EpiMode : int { EPI_F32 = 0, EPI_QKV = 1, EPI_RESID = 2, EPI_SWIGLU = 3 };
+// EPI_PARTIAL (tensor-core GEMM only): every CTA writes its fp32 partial
+// tile(s) to the workspace and a separate kernel reduces them.
+enum EpiMode : int { EPI_F32 = 0, EPI_QKV = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_PARTIAL = 4 };
 
 struct EpiParams {
     int mode;

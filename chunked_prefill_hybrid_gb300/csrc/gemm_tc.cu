@@ -54,7 +54,8 @@ struct TcArgs {
     int units, grid, stages;
     uint32_t tmem_cols;
     int n_acc;          // accumulator buffers (2 when one sub-tile fits twice)
-    float *ws;          // [grid][2][tg][128]
+    int slots;          // partial tiles per CTA in the workspace
+    float *ws;          // [grid][slots][tg][128]
     int *counters;      // [n_mtiles * n_groups]
 };
 
@@ -217,7 +218,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int buf = seg % a.n_acc;
             const int use = seg / a.n_acc;
             const bool whole = (kb0 == 0 && kb1 == a.nkb);
-            if (whole && ep.mode == EPI_RESID) {
+            const bool partial_mode = ep.mode == EPI_PARTIAL;
+            const bool direct = whole && !partial_mode;
+            if (direct && ep.mode == EPI_RESID) {
                 // bring this tile's residual rows into L2 while the MMAs run
                 for (int i = et; i < a.tg * 2; i += 128) {
                     const int t = g * a.tg + (i >> 1);
@@ -234,8 +237,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
-            const int slot = (u == u0) ? 0 : 1;
-            float *ws_mine = a.ws + ((size_t)cta * 2 + slot) * a.tg * TC_BM;
+            const int slot = tile - u0 / a.nkb;
+            float *ws_mine = a.ws + ((size_t)cta * a.slots + slot) * a.tg * TC_BM;
             for (int sub = 0; sub < a.nsub; ++sub) {
                 for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
 #pragma unroll
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 v[4 * e + 2] = f.z;
                                 v[4 * e + 3] = f.w;
                             }
-                            if (whole) {
+                            if (direct) {
                                 const int t = g * a.tg + col, n0 = mt * TC_BM + gq * 16;
                                 if (t < a.T && n0 < a.N)
                                     epi_group(ep, t, n0, v);
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&acce[buf]);
-            if (!whole) {
+            if (!whole && !partial_mode) {
                 // stream-K fixup: the last contributor to arrive finishes the tile
                 __threadfence();
                 epi_bar();
@@ -307,9 +310,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int e = 0; e < 16; ++e)
                             v[e] = 0.f;
                         for (int c = c_lo; c <= c_hi; ++c) {
-                            const int cslot = (unit_begin(c, a) / a.nkb == tile) ? 0 : 1;
+                            const int cslot = tile - unit_begin(c, a) / a.nkb;
                             const float4 *src = reinterpret_cast<const float4 *>(
-                                a.ws + (((size_t)c * 2 + cslot) * a.tg + col) * TC_BM + gq * 16);
+                                a.ws + (((size_t)c * a.slots + cslot) * a.tg + col) * TC_BM + gq * 16);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float4 f = __ldcg(src + e);
@@ -437,15 +440,40 @@ TcShape tc_shape(int T)
     return sh;
 }
 
-size_t tc_workspace_floats(int num_sms, int max_tokens)
+// Slots (partial tiles) a CTA can hold: the most tiles any CTA's unit range touches.
+static int tc_slots(long long units, int grid, int nkb)
 {
-    const TcShape sh = tc_shape(max_tokens < 512 ? max_tokens : 512);
-    const int tg = sh.tg < 512 ? 512 : sh.tg;
-    return (size_t)num_sms * 2 * tg * TC_BM;
+    const long long per = (units + grid - 1) / grid;
+    return (int)((per + nkb - 1) / nkb + 1);
+}
+
+static void tc_partition_dims(int T, int N, int K, int num_sms, int &grid, long long &units, int &nkb, int &tg)
+{
+    const TcShape sh = tc_shape(T);
+    const int n_mtiles = (N + TC_BM - 1) / TC_BM;
+    nkb = (K + TC_BK - 1) / TC_BK;
+    units = (long long)n_mtiles * sh.n_groups * nkb;
+    grid = (int)(units < num_sms ? units : num_sms);
+    tg = sh.tg;
+}
+
+size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes)
+{
+    size_t need = 0;
+    for (int i = 0; i < n_shapes; ++i)
+        for (int T = 1; T <= max_tokens; ++T) {
+            int grid, nkb, tg;
+            long long units;
+            tc_partition_dims(T, Ns[i], Ks[i], num_sms, grid, units, nkb, tg);
+            const size_t n = (size_t)grid * tc_slots(units, grid, nkb) * tg * TC_BM;
+            if (n > need)
+                need = n;
+        }
+    return need;
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, int K, const EpiParams &ep,
-                           const TcRuntime &rt, cudaStream_t s)
+                           const TcRuntime &rt, cudaStream_t s, TcPartition *part)
 {
     if (T <= 0)
         return cudaSuccess;
@@ -467,8 +495,18 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, 
         return cudaErrorInvalidValue;
     a.units = (int)units;
     a.grid = (int)(units < rt.num_sms ? units : rt.num_sms);
-    if ((size_t)a.grid * 2 * a.tg * TC_BM > rt.ws_floats)
+    a.slots = tc_slots(units, a.grid, a.nkb);
+    if ((size_t)a.grid * a.slots * a.tg * TC_BM > rt.ws_floats)
         return cudaErrorInvalidValue;
+    if (part) {
+        part->ws = rt.ws;
+        part->grid = a.grid;
+        part->units = a.units;
+        part->nkb = a.nkb;
+        part->n_groups = a.n_groups;
+        part->tg = a.tg;
+        part->slots = a.slots;
+    }
     a.n_acc = (a.nsub == 1) ? 2 : 1;
     a.tmem_cols = 512;  // two accumulators at columns 0 and 256
     a.ws = rt.ws;

@@ -23,7 +23,19 @@ struct TcRuntime {
     int n_counters = 0;
 };
 
-size_t tc_workspace_floats(int num_sms, int max_tokens);
+// Where each CTA of one launch left its fp32 partial tiles: tile `tile`
+// (= m_tile * n_groups + token group) covers units [tile*nkb, tile*nkb+nkb)
+// of an even split of `units` over `grid` CTAs; CTA c keeps its share of
+// tile at slot (tile - first tile of c), element [col][row] of
+// ws + ((c * slots + slot) * tg) * 128.
+struct TcPartition {
+    const float *ws = nullptr;
+    int grid = 0, units = 0, nkb = 0, n_groups = 0, tg = 0, slots = 0;
+};
+
+// Workspace floats needed for any batch of up to max_tokens rows and the
+// given (N, K) shapes.
+size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes);
 
 // Weights in the tiled layout [n_tile][k_block][128][64] (zero padded).
 size_t tiled_weight_elems(int N, int K);
@@ -35,6 +47,11 @@ bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K);
 // acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
 // tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).
 cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, int K, const EpiParams &ep,
-                           const TcRuntime &rt, cudaStream_t s);
+                           const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr);
+
+// out = bf16(resid + sum of the partial tiles of `part`) for T x N outputs;
+// if gamma: norm_out = bf16(out * rsqrt(mean(out^2) + eps) * gamma) per row.
+cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16 *resid, bf16 *out,
+                               const float *gamma, bf16 *norm_out, float eps, cudaStream_t s);
 
 }  // namespace hb

@@ -49,7 +49,15 @@ int hb_init_fast_path(hb_ctx *ctx)
     if (cudaDeviceGetAttribute(&rt.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device) != cudaSuccess)
         return ctx->set_error(HB_ECUDA, "cudaDeviceGetAttribute failed");
     rt.num_sms = ctx->num_sms;
-    rt.ws_floats = tc_workspace_floats(ctx->num_sms, ctx->cfg.max_tokens);
+    {
+        const hb_model_config &c = ctx->cfg;
+        const int Ns[4] = {ctx->n_qkv, c.hidden, ctx->n_gu, c.hidden};
+        const int Ks[4] = {c.hidden, c.n_heads * c.head_dim, c.hidden, c.ffn};
+        rt.ws_floats = tc_workspace_floats(ctx->num_sms, c.max_tokens, Ns, Ks, 4);
+        const size_t floor_floats = (size_t)ctx->num_sms * 2 * 512 * 128;  // room for hb_gemm_test shapes
+        if (rt.ws_floats < floor_floats)
+            rt.ws_floats = floor_floats;
+    }
     rt.n_counters = 8192;
     if (cudaMalloc((void **)&rt.ws, rt.ws_floats * sizeof(float)) != cudaSuccess ||
         cudaMalloc((void **)&rt.counters, rt.n_counters * sizeof(int)) != cudaSuccess) {
@@ -139,15 +147,25 @@ static cudaError_t gemm(hb_ctx *ctx, const CUtensorMap *tmW, const bf16 *X, cons
     return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
 }
 
-int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
+// One decoder layer.  On the tensor-core path the O-proj and down-proj
+// GEMMs leave split-K partials that one kernel per token finishes together
+// with the residual add and the next RMSNorm (norm-2, and norm-1 of the next
+// layer), so a layer is 7 launches: [norm-1 for the first layer only],
+// QKV GEMM (RoPE + KV append), attention, O GEMM, reduce+residual+norm-2,
+// gate/up GEMM (SwiGLU), down GEMM, reduce+residual(+next norm-1).
+int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, const bf16 *x, bf16 *y)
 {
     const hb_model_config &c = ctx->cfg;
     const LayerDev &L = ctx->layers[l];
     const LayerMaps &M = ctx->fast->maps[l];
     const int T = b.T, H = c.hidden, d = c.head_dim;
     cudaStream_t s = ctx->stream;
+    const bool tc = ctx->gemm_impl == 1;
 
-    LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s));
+    // on the tensor-core path norm-1 of every layer but the first was
+    // produced by the previous layer's final reduce
+    if (!tc || l == l_first)
+        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s));
 
     EpiParams ep{};
     ep.mode = EPI_QKV;
@@ -190,6 +208,29 @@ int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
            launch_attention_simple(ctx->q, L.k_pool, L.v_pool, b, c.n_heads, c.n_kv_heads, d, ctx->attn_o, s));
     }
 
+    EpiParams eg{};
+    eg.mode = EPI_SWIGLU;
+    eg.T = T;
+    eg.N = ctx->n_gu;
+    eg.act = ctx->act;
+    eg.ffn = c.ffn;
+
+    if (tc) {
+        const TcRuntime &rt = ctx->fast->rt;
+        EpiParams pp{};
+        pp.mode = EPI_PARTIAL;
+        pp.T = T;
+        pp.N = H;
+        TcPartition part;
+        LK(K_GEMM_O, launch_gemm_tc(M.o, ctx->attn_o, T, H, c.n_heads * d, pp, rt, s, &part));
+        LK(K_REDUCE_NORM, launch_reduce_norm(part, T, H, x, ctx->h, L.g2, ctx->xn, c.rms_eps, s));
+        LK(K_GEMM_GATE_UP, launch_gemm_tc(M.gu, ctx->xn, T, ctx->n_gu, H, eg, rt, s));
+        LK(K_GEMM_DOWN, launch_gemm_tc(M.d, ctx->act, T, H, c.ffn, pp, rt, s, &part));
+        const float *g_next = (l + 1 < l_last) ? ctx->layers[l + 1].g1 : nullptr;
+        LK(K_REDUCE_NORM, launch_reduce_norm(part, T, H, ctx->h, y, g_next, ctx->xn, c.rms_eps, s));
+        return HB_OK;
+    }
+
     EpiParams eo{};
     eo.mode = EPI_RESID;
     eo.T = T;
@@ -200,12 +241,6 @@ int run_layer(hb_ctx *ctx, int l, const BatchDev &b, const bf16 *x, bf16 *y)
 
     LK(K_RMSNORM, launch_rmsnorm(ctx->h, L.g2, ctx->xn, T, H, c.rms_eps, s));
 
-    EpiParams eg{};
-    eg.mode = EPI_SWIGLU;
-    eg.T = T;
-    eg.N = ctx->n_gu;
-    eg.act = ctx->act;
-    eg.ffn = c.ffn;
     LK(K_GEMM_GATE_UP, gemm(ctx, &M.gu, ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
 
     EpiParams ed{};

@@ -550,7 +550,7 @@ static int run_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, co
     const bf16 *x = (const bf16 *)x_in;
     for (int l = l0; l < l1; ++l) {
         bf16 *y = (l == l1 - 1) ? (bf16 *)x_out : ((l - l0) % 2 == 0 ? ctx->xa : ctx->xb);
-        if ((rc = run_layer(ctx, l, b, x, y)))
+        if ((rc = run_layer(ctx, l, l0, l1, b, x, y)))
             return rc;
         x = y;
     }

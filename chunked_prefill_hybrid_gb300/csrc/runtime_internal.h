@@ -43,11 +43,12 @@ enum Kind : int {
     K_GEMM_DOWN,
     K_KVIO,
     K_GEMM_TEST,
+    K_REDUCE_NORM,
     K_NUM_KINDS
 };
-static const char *const kKindNames[K_NUM_KINDS] = {"rmsnorm",   "gemm_qkv",       "attention",
-                                                     "attn_combine", "gemm_o",     "gemm_gate_up",
-                                                     "gemm_down", "kv_io",          "gemm_test"};
+static const char *const kKindNames[K_NUM_KINDS] = {"rmsnorm",   "gemm_qkv",  "attention", "attn_combine",
+                                                     "gemm_o",    "gemm_gate_up", "gemm_down", "kv_io",
+                                                     "gemm_test", "reduce_norm"};
 
 constexpr int kMetaRing = 4;
 
@@ -105,4 +106,4 @@ struct hb_ctx {
 int hb_init_fast_path(hb_ctx *ctx);
 void hb_free_fast_path(hb_ctx *ctx);
 int hb_plan_fast_path(hb_ctx *ctx, const hb::Plan &p, int *hm, size_t &at, hb::BatchDev &b);
-int run_layer(hb_ctx *ctx, int l, const hb::BatchDev &b, const hb::bf16 *x, hb::bf16 *y);
+int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const hb::BatchDev &b, const hb::bf16 *x, hb::bf16 *y);
