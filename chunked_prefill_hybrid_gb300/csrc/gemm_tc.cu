@@ -50,8 +50,11 @@ constexpr uint64_t TC_WAIT_NS = 2000000000ull;  // 2 s
 struct TcArgs {
     int T, N, K;
     int n_mtiles, nkb, n_groups;
+    int cl;             // CTAs per cluster: neighbouring weight tiles sharing one multicast X tile
+    int n_quads;        // groups of cl weight tiles
     int tg, nsub, n_sub;
-    int units, grid, stages;
+    int piece, box_rows;  // X rows each CTA fetches per stage, in boxes of box_rows
+    int units, grid, stages;  // units over (tile group, token group, k-block); grid = clusters
     uint32_t tmem_cols;
     int n_acc;          // accumulator buffers (2 when one sub-tile fits twice)
     int slots;          // partial tiles per CTA in the workspace
@@ -101,13 +104,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     float *stg = (float *)(smem + (size_t)S * stage_bytes + 256);  // [32][TC_STG_LD]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cta = blockIdx.x;
-    const int u0 = unit_begin(cta, a), u1 = unit_begin(cta + 1, a);
+    const int rank = a.cl > 1 ? (int)cluster_ctarank() : 0;
+    const int clu = blockIdx.x / a.cl;       // cluster index, the unit owner
+    const int cta = clu * a.cl + rank;       // workspace index
+    const uint16_t mask = (uint16_t)((1u << a.cl) - 1u);
+    const int u0 = unit_begin(clu, a), u1 = unit_begin(clu + 1, a);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], a.cl);  // released by the MMA of every CTA of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
@@ -123,17 +129,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tmem_alloc(tmem_slot, a.tmem_cols);
     tc_fence_before();
     __syncthreads();
+    if (a.cl > 1)
+        cluster_sync();  // peers' barriers are initialised before any multicast lands
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ producer
-        const uint32_t bytes = (uint32_t)stage_bytes;
+        // W: this CTA's own 128-row tile.  X: the stage's tg token rows;
+        // CTA `rank` fetches `piece` rows starting at min(rank * piece,
+        // tg - piece) and multicasts them to the whole cluster (slices may
+        // overlap at the end; overlapping rows carry identical data and are
+        // counted in the expected bytes).
+        const uint32_t bytes = (uint32_t)(TC_W_BYTES + a.cl * a.piece * TC_BK * 2);
+        const int row0 = min(rank * a.piece, a.tg - a.piece);
         int it = 0;
         bool ok = true;
         for (int u = u0; u < u1 && ok; ++u, ++it) {
-            const int tile = u / a.nkb, kb = u % a.nkb;
-            const int mt = tile / a.n_groups, g = tile % a.n_groups;
+            const int qt = u / a.nkb, kb = u % a.nkb;
+            const int mt = (qt / a.n_groups) * a.cl + rank, g = qt % a.n_groups;
             const int s = it % S;
             if (it >= S && !mbar_wait(&empty[s], ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, TC_WAIT_NS)) {
                 set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
@@ -144,10 +158,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint8_t *sw = smem + (size_t)s * stage_bytes;
             mbar_expect_tx(&full[s], bytes);
             tma_load_2d(sw, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM);
-            for (int sub = 0; sub < a.nsub; ++sub)
-                tma_load_2d(sw + TC_W_BYTES + sub * a.n_sub * TC_BK * 2, &tmX, &full[s], kb * TC_BK,
-                            g * a.tg + sub * a.n_sub);
+            for (int r = row0; r < row0 + a.piece; r += a.box_rows) {
+                uint8_t *dst = sw + TC_W_BYTES + r * TC_BK * 2;
+                if (a.cl > 1)
+                    tma_load_2d_multicast(dst, &tmX, &full[s], kb * TC_BK, g * a.tg + r, mask);
+                else
+                    tma_load_2d(dst, &tmX, &full[s], kb * TC_BK, g * a.tg + r);
+            }
         }
+        // tail: wait until every CTA of the cluster released the last use of
+        // each stage, so no arrival or multicast write is still in flight to
+        // this CTA's shared memory when it exits
+        for (int k = (it > S ? it - S : 0); k < it; ++k)
+            mbar_wait(&empty[k % S], (uint32_t)(k / S) & 1u, ok ? abort_flag : nullptr, ok ? TC_WAIT_NS : TC_WAIT_NS / 4);
         if (!ok) {
             for (int k = (it > S ? it - S : 0); k < it; ++k)
                 mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u, nullptr, TC_WAIT_NS / 4);
@@ -189,7 +212,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         mma_bf16(d0 + (uint32_t)(sub * 256), ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                 }
-                mma_commit(&empty[s]);
+                if (a.cl > 1)
+                    mma_commit_multicast(&empty[s], mask);
+                else
+                    mma_commit(&empty[s]);
             }
             if (!ok)
                 break;
@@ -212,9 +238,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         int seg = 0;
         for (int u = u0; u < u1; ++seg) {
-            const int tile = u / a.nkb, kb0 = u % a.nkb;
+            const int qt = u / a.nkb, kb0 = u % a.nkb;
             const int kb1 = min(a.nkb, kb0 + (u1 - u));
-            const int mt = tile / a.n_groups, g = tile % a.n_groups;
+            const int mt = (qt / a.n_groups) * a.cl + rank, g = qt % a.n_groups;
+            const int tile = mt * a.n_groups + g;  // counters
             const int buf = seg % a.n_acc;
             const int use = seg / a.n_acc;
             const bool whole = (kb0 == 0 && kb1 == a.nkb);
@@ -237,7 +264,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
-            const int slot = tile - u0 / a.nkb;
+            const int slot = qt - u0 / a.nkb;
             float *ws_mine = a.ws + ((size_t)cta * a.slots + slot) * a.tg * TC_BM;
             for (int sub = 0; sub < a.nsub; ++sub) {
                 for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
@@ -291,8 +318,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // stream-K fixup: the last contributor to arrive finishes the tile
                 __threadfence();
                 epi_bar();
-                const int c_lo = unit_owner((long long)tile * a.nkb, a);
-                const int c_hi = unit_owner((long long)tile * a.nkb + a.nkb - 1, a);
+                const int c_lo = unit_owner((long long)qt * a.nkb, a);
+                const int c_hi = unit_owner((long long)qt * a.nkb + a.nkb - 1, a);
                 if (et == 0) {
                     const int old = atomicAdd(&a.counters[tile], 1);
                     *last_flag = (old == c_hi - c_lo);
@@ -310,9 +337,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int e = 0; e < 16; ++e)
                             v[e] = 0.f;
                         for (int c = c_lo; c <= c_hi; ++c) {
-                            const int cslot = tile - unit_begin(c, a) / a.nkb;
+                            const int cslot = qt - unit_begin(c, a) / a.nkb;
                             const float4 *src = reinterpret_cast<const float4 *>(
-                                a.ws + (((size_t)c * a.slots + cslot) * a.tg + col) * TC_BM + gq * 16);
+                                a.ws + (((size_t)(c * a.cl + rank) * a.slots + cslot) * a.tg + col) * TC_BM + gq * 16);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float4 f = __ldcg(src + e);
@@ -334,6 +361,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (a.cl > 1)
+        cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, a.tmem_cols);
@@ -447,13 +476,23 @@ static int tc_slots(long long units, int grid, int nkb)
     return (int)((per + nkb - 1) / nkb + 1);
 }
 
-static void tc_partition_dims(int T, int N, int K, int num_sms, int &grid, long long &units, int &nkb, int &tg)
+static int tc_cluster_for(int n_mtiles, int forced)
+{
+    if (forced > 0)
+        return forced;
+    return n_mtiles >= 8 ? 4 : (n_mtiles >= 2 ? 2 : 1);
+}
+
+static void tc_partition_dims(int T, int N, int K, int num_sms, int cl, int &grid, long long &units, int &nkb,
+                              int &tg)
 {
     const TcShape sh = tc_shape(T);
     const int n_mtiles = (N + TC_BM - 1) / TC_BM;
+    const int n_quads = (n_mtiles + cl - 1) / cl;
     nkb = (K + TC_BK - 1) / TC_BK;
-    units = (long long)n_mtiles * sh.n_groups * nkb;
-    grid = (int)(units < num_sms ? units : num_sms);
+    units = (long long)n_quads * sh.n_groups * nkb;
+    const int max_clusters = num_sms / cl;
+    grid = (int)(units < max_clusters ? units : max_clusters);
     tg = sh.tg;
 }
 
@@ -462,12 +501,14 @@ size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int
     size_t need = 0;
     for (int i = 0; i < n_shapes; ++i)
         for (int T = 1; T <= max_tokens; ++T) {
-            int grid, nkb, tg;
-            long long units;
-            tc_partition_dims(T, Ns[i], Ks[i], num_sms, grid, units, nkb, tg);
-            const size_t n = (size_t)grid * tc_slots(units, grid, nkb) * tg * TC_BM;
-            if (n > need)
-                need = n;
+            for (int cl = 1; cl <= 4; cl *= 2) {
+                int grid, nkb, tg;
+                long long units;
+                tc_partition_dims(T, Ns[i], Ks[i], num_sms, cl, grid, units, nkb, tg);
+                const size_t n = (size_t)grid * cl * tc_slots(units, grid, nkb) * tg * TC_BM;
+                if (n > need)
+                    need = n;
+            }
         }
     return need;
 }
@@ -490,17 +531,66 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, 
     a.tg = sh.tg;
     a.nsub = sh.nsub;
     a.n_sub = sh.n_sub;
-    const long long units = (long long)a.n_mtiles * a.n_groups * a.nkb;
-    if (units > (1ll << 30) || (long long)a.n_mtiles * a.n_groups > rt.n_counters)
+    a.cl = tc_cluster_for(a.n_mtiles, rt.cluster);
+    a.n_quads = (a.n_mtiles + a.cl - 1) / a.cl;
+    {
+        int piece = (a.tg + a.cl - 1) / a.cl;
+        piece = (piece + 7) / 8 * 8;  // whole 1 KB swizzle atoms
+        if (piece < 8)
+            piece = 8;
+        if (piece > a.tg)
+            piece = a.tg;
+        a.piece = piece;
+        a.box_rows = piece <= 256 ? piece : piece / 2;  // tg <= 512, a multiple of 32 when > 256
+    }
+    const long long units = (long long)a.n_quads * a.n_groups * a.nkb;
+    if (units > (1ll << 30) || (long long)a.n_quads * a.cl * a.n_groups > rt.n_counters)
         return cudaErrorInvalidValue;
     a.units = (int)units;
-    a.grid = (int)(units < rt.num_sms ? units : rt.num_sms);
+    int stages = 10;
+    while (stages > 2 && tc_smem_bytes(a.tg, stages) > rt.max_smem)
+        --stages;
+    if (tc_smem_bytes(a.tg, stages) > rt.max_smem)
+        return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    const int smem = tc_smem_bytes(a.tg, stages);
+    static int configured = 0;
+    if (configured < rt.max_smem) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, rt.max_smem);
+        if (e != cudaSuccess)
+            return e;
+        configured = rt.max_smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // clusters that can be resident at once (cached per cluster size)
+    static int max_clusters[5] = {0, 0, 0, 0, 0};
+    if (!max_clusters[a.cl]) {
+        cfg.gridDim = dim3((unsigned)(rt.num_sms / a.cl * a.cl));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = rt.num_sms / a.cl;
+        }
+        max_clusters[a.cl] = n;
+    }
+    a.grid = (int)(units < max_clusters[a.cl] ? units : max_clusters[a.cl]);
     a.slots = tc_slots(units, a.grid, a.nkb);
-    if ((size_t)a.grid * a.slots * a.tg * TC_BM > rt.ws_floats)
+    if ((size_t)a.grid * a.cl * a.slots * a.tg * TC_BM > rt.ws_floats)
         return cudaErrorInvalidValue;
     if (part) {
         part->ws = rt.ws;
         part->grid = a.grid;
+        part->cl = a.cl;
         part->units = a.units;
         part->nkb = a.nkb;
         part->n_groups = a.n_groups;
@@ -511,23 +601,13 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, 
     a.tmem_cols = 512;  // two accumulators at columns 0 and 256
     a.ws = rt.ws;
     a.counters = rt.counters;
-    int stages = 10;
-    while (stages > 2 && tc_smem_bytes(a.tg, stages) > rt.max_smem)
-        --stages;
-    if (tc_smem_bytes(a.tg, stages) > rt.max_smem)
-        return cudaErrorInvalidConfiguration;
-    a.stages = stages;
     CUtensorMap tmX;
-    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.n_sub))
+    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.box_rows))
         return cudaErrorInvalidValue;
-    static int configured = 0;
-    if (configured < rt.max_smem) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, rt.max_smem);
-        if (e != cudaSuccess)
-            return e;
-        configured = rt.max_smem;
-    }
-    k_gemm_tc<<<a.grid, TC_THREADS, tc_smem_bytes(a.tg, stages), s>>>(tmW, tmX, a, ep);
+    cfg.gridDim = dim3((unsigned)(a.grid * a.cl));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, tmW, tmX, a, ep);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

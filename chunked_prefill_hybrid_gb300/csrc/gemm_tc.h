@@ -21,16 +21,18 @@ struct TcRuntime {
     size_t ws_floats = 0;
     int *counters = nullptr;  // per-tile arrival counters, zero between launches
     int n_counters = 0;
+    int cluster = 0;          // CTAs per cluster (0: chosen per shape; 1, 2 or 4 forced)
 };
 
-// Where each CTA of one launch left its fp32 partial tiles: tile `tile`
-// (= m_tile * n_groups + token group) covers units [tile*nkb, tile*nkb+nkb)
-// of an even split of `units` over `grid` CTAs; CTA c keeps its share of
-// tile at slot (tile - first tile of c), element [col][row] of
-// ws + ((c * slots + slot) * tg) * 128.
+// Where each CTA of one launch left its fp32 partial tiles.  Weight tiles
+// are grouped cl at a time (one cluster); group tile qt = (m_tile / cl) *
+// n_groups + token group covers units [qt*nkb, qt*nkb+nkb) of an even split
+// of `units` over `grid` clusters.  Cluster c's CTA of rank m_tile % cl keeps
+// its share at slot (qt - first group tile of c), element [col][row] of
+// ws + (((c * cl + rank) * slots + slot) * tg) * 128.
 struct TcPartition {
     const float *ws = nullptr;
-    int grid = 0, units = 0, nkb = 0, n_groups = 0, tg = 0, slots = 0;
+    int grid = 0, cl = 1, units = 0, nkb = 0, n_groups = 0, tg = 0, slots = 0;
 };
 
 // Workspace floats needed for any batch of up to max_tokens rows and the

@@ -142,7 +142,7 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
 static cudaError_t gemm(hb_ctx *ctx, const CUtensorMap *tmW, const bf16 *X, const bf16 *W, int T, int N, int K,
                         const EpiParams &ep)
 {
-    if (ctx->gemm_impl == 1)
+    if (ctx->gemm_impl >= 1)
         return launch_gemm_tc(*tmW, X, T, N, K, ep, ctx->fast->rt, ctx->stream);
     return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
 }
@@ -160,7 +160,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     const LayerMaps &M = ctx->fast->maps[l];
     const int T = b.T, H = c.hidden, d = c.head_dim;
     cudaStream_t s = ctx->stream;
-    const bool tc = ctx->gemm_impl == 1;
+    const bool tc = ctx->gemm_impl >= 1;
 
     // on the tensor-core path norm-1 of every layer but the first was
     // produced by the previous layer's final reduce
@@ -295,9 +295,11 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
 {
     if (!ctx)
         return HB_EINVAL;
-    if (gemm_impl < 0 || gemm_impl > 1 || attn_impl < 0 || attn_impl > 1)
-        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl and attn_impl must be 0 or 1");
+    if (gemm_impl < 0 || gemm_impl > 4 || attn_impl < 0 || attn_impl > 1)
+        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0..4 and attn_impl 0 or 1");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
+    // 1: cluster size chosen per shape; 2, 3, 4: clusters of 1, 2, 4 CTAs
+    ctx->fast->rt.cluster = gemm_impl >= 2 ? (1 << (gemm_impl - 2)) : 0;
     return HB_OK;
 }

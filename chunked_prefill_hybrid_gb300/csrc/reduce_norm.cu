@@ -43,18 +43,18 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
         const int n0 = (threadIdx.x + i * RN_THREADS) * 8;
         if (n0 >= a.N)
             break;
-        const int mt = n0 >> 7;
-        const int tile = mt * p.n_groups + g;
-        const long long u0 = (long long)tile * p.nkb;
+        const int mt = n0 >> 7, rank = mt % p.cl;
+        const int qt = (mt / p.cl) * p.n_groups + g;
+        const long long u0 = (long long)qt * p.nkb;
         const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
         float acc[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             acc[k] = 0.f;
         for (int c = c_lo; c <= c_hi; ++c) {
-            const int slot = tile - ubegin(c, p) / p.nkb;
-            const float4 *src =
-                reinterpret_cast<const float4 *>(p.ws + (((size_t)c * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
+            const int slot = qt - ubegin(c, p) / p.nkb;
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.ws + ((((size_t)c * p.cl + rank) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
             const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
             acc[0] += x0.x;
             acc[1] += x0.y;
