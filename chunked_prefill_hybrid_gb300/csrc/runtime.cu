@@ -22,7 +22,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/hb.h"
+#include "hb.h"
 #include "gemm_tc.h"
 #include "kernels.h"
 #include "runtime_internal.h"

@@ -9,7 +9,7 @@
 #include <utility>
 #include <vector>
 
-#include "../../include/hb.h"
+#include "hb.h"
 #include "common.cuh"
 
 namespace hb {
