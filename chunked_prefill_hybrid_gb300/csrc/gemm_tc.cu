@@ -5,28 +5,32 @@
 // section 3.4 "Decode-Maximal Batching", "How fusion works").
 //
 // Orientation ("swap AB"): the MMA's M is 128 weight rows (output features)
-// and its N is the batch's tokens, a multiple of 16.  A CTA holds every token
-// of the batch for its weight tile (up to 512 tokens as two MMAs of N <= 256
-// into two TMEM accumulators), so T = 256 + 18 = 274 runs as 2 x 144 columns
-// (5% padding) -- the tile-quantization effect of SARATHI summary section
-// 3.4 / Figure 7 is kept small by sizing the token tile to T rather than
-// to a fixed 128.
+// and its N is a group of the batch's tokens, a multiple of 16 up to 256.  A
+// batch of T rows is cut into G = ceil(T / 256) equal token groups, so
+// T = 256 + 18 = 274 runs as 2 x 144 columns (5% padding) instead of three
+// 128-row tiles (29%) -- the tile-quantization effect of SARATHI summary
+// section 3.4 / Figure 7 is kept small by sizing the token tile to T.
+//
+// The G CTAs that handle the G token groups of one weight tile form a
+// thread-block cluster: each fetches a slice of the weight tile and
+// multicasts it to all of them, so every weight byte still leaves HBM once.
 //
 // Weights are stored tiled, [n_tile][k_block][128][64], so every TMA box is
-// one contiguous 16 KB run of HBM and each CTA streams a contiguous range.
+// a contiguous run of HBM and each cluster streams a contiguous range.
 //
 // Work split ("stream-K"): the (weight tile, k-block) units are divided
-// evenly over a persistent grid of one CTA per SM.  A tile whose k-range
-// spans several CTAs is finished by the last of them to arrive (per-tile
-// arrival counter, no waiting): it sums every contributor's fp32 partial in
-// CTA order -- a fixed order, so results do not depend on timing -- and runs
-// the fused epilogue.
+// evenly over a persistent grid of clusters, one CTA per SM.  A tile whose
+// k-range spans several clusters is finished either by the last CTA to
+// arrive (per-tile arrival counter, no waiting), which sums every
+// contributor's fp32 partial in cluster order -- a fixed order, so results
+// do not depend on timing -- or, in partial mode, by a separate kernel.
 //
-//   warp 0      TMA producer: W box [128][64], X boxes [n_sub][64]
-//   warp 1      TMEM owner; one thread issues tcgen05.mma (K = 16, 4 per
-//               k-block per sub-tile) and commits stage / accumulator barriers
+//   warp 0      TMA producer: W slice (multicast) and this CTA's X tokens
+//   warp 1      TMEM owner; one thread issues tcgen05.mma (M=128, N=n_sub,
+//               K=16, 4 per k-block) into one of two TMEM accumulators
 //   warps 2..5  epilogue: tcgen05.ld (one TMEM lane = one output feature,
-//               columns = tokens), fused epilogue or partial write + fixup
+//               columns = tokens), transposed through shared memory, fused
+//               epilogue on (token, 16 features) with 16-byte accesses
 // Every mbarrier wait is bounded (wall clock); on a timeout the kernel
 // records an error in the device error word, drains and frees TMEM.
 #include <cuda.h>
@@ -46,20 +50,60 @@ constexpr int TC_BK = 64;
 constexpr int TC_THREADS = 192;
 constexpr int TC_W_BYTES = TC_BM * TC_BK * 2;
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;  // 2 s
+constexpr int TC_MAX_G = 8;
 
 struct TcArgs {
     int T, N, K;
-    int n_mtiles, nkb, n_groups;
-    int cl;             // CTAs per cluster: neighbouring weight tiles sharing one multicast X tile
-    int n_quads;        // groups of cl weight tiles
-    int tg, nsub, n_sub;
-    int piece, box_rows;  // X rows each CTA fetches per stage, in boxes of box_rows
-    int units, grid, stages;  // units over (tile group, token group, k-block); grid = clusters
-    uint32_t tmem_cols;
-    int n_acc;          // accumulator buffers (2 when one sub-tile fits twice)
-    int slots;          // partial tiles per CTA in the workspace
-    float *ws;          // [grid][slots][tg][128]
-    int *counters;      // [n_mtiles * n_groups]
+    int n_mtiles, nkb;
+    int G;            // token groups = CTAs per cluster
+    int nsub;         // MMAs per k-block (1 or 2; the second accumulates at TMEM column 256)
+    int n_sub;        // tokens per MMA (multiple of 16, <= 256); a CTA holds tg = nsub * n_sub
+    int tg;
+    int wpiece;       // weight-tile rows each CTA fetches and multicasts
+    int units, grid;  // units = n_mtiles * nkb over `grid` clusters
+    int stages, slots;
+    float *ws;        // [grid * G][slots][tg][128]
+    int *counters;    // [n_mtiles * G]
+    const bf16 *w_tiled;  // the weights, streamed into L2 ahead of the TMA loads
+    int rel;              // stages released per commit: 2 when the MMAs are short (N < 224), else 1
+};
+
+// A cluster's unit range [u0, u1) is cut at tile boundaries into segments
+// (one accumulator each).  They are processed with the split tiles first --
+// the range's last segment, then its first -- and the whole tiles after, so
+// that the stream-K fixups of split tiles overlap the remaining work.
+// Distance (k-blocks of 16 KB) the weight stream is prefetched into L2 ahead
+// of its TMA loads; the loads then find their data in L2, so fewer shared-
+// memory stages cover the HBM latency.
+constexpr int TC_PREFETCH = 12;
+
+struct SegIter {
+    int u0, u1, nkb, n;
+    __device__ SegIter(int u0_, int u1_, int nkb_) : u0(u0_), u1(u1_), nkb(nkb_)
+    {
+        n = (u1 > u0) ? ((u1 - 1) / nkb - u0 / nkb + 1) : 0;
+    }
+    // bounds of the segment covering tile index `t` (u0 / nkb <= t)
+    __device__ void tile_seg(int t, int &a, int &b) const
+    {
+        a = max(u0, t * nkb);
+        b = min(u1, (t + 1) * nkb);
+    }
+    // i-th segment in processing order
+    __device__ void get(int i, int &a, int &b) const
+    {
+        const int t0 = u0 / nkb;
+        int t;
+        if (n == 1)
+            t = t0;
+        else if (i == 0)
+            t = t0 + n - 1;
+        else if (i == 1)
+            t = t0;
+        else
+            t = t0 + i - 1;
+        tile_seg(t, a, b);
+    }
 };
 
 // Epilogue staging tile: 32 token columns x 128 features, fp32, padded rows.
@@ -94,9 +138,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int S = a.stages;
     const int stage_bytes = tc_stage_bytes(a.tg);
     uint64_t *full = (uint64_t *)(smem + (size_t)S * stage_bytes);
-    uint64_t *empty = full + S;
-    uint64_t *accf = empty + S;       // [2]
-    uint64_t *acce = accf + 2;        // [2]
+    uint64_t *empty = full + S;  // one per group of `rel` consecutive stages
+    uint64_t *accf = empty + S;  // [2]
+    uint64_t *acce = accf + 2;   // [2]
     uint64_t *drain = acce + 2;
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
@@ -104,17 +148,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     float *stg = (float *)(smem + (size_t)S * stage_bytes + 256);  // [32][TC_STG_LD]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = a.cl > 1 ? (int)cluster_ctarank() : 0;
-    const int clu = blockIdx.x / a.cl;       // cluster index, the unit owner
-    const int cta = clu * a.cl + rank;       // workspace index
-    const uint16_t mask = (uint16_t)((1u << a.cl) - 1u);
+    const int rank = a.G > 1 ? (int)cluster_ctarank() : 0;  // token group of this CTA
+    const int clu = blockIdx.x / a.G;                        // cluster: the unit owner
+    const int cta = clu * a.G + rank;                        // workspace index
+    const uint16_t mask = (uint16_t)((1u << a.G) - 1u);
     const int u0 = unit_begin(clu, a), u1 = unit_begin(clu + 1, a);
+    const int t_base = rank * a.tg;
+    const int n_acc = a.nsub == 1 ? 2 : 1;  // accumulator buffers
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < S; ++s)
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], a.cl);  // released by the MMA of every CTA of the cluster
-        }
+        for (int s = 0; s < S / a.rel; ++s)
+            mbar_init(&empty[s], a.G);  // released by the MMA of every CTA of the cluster
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accf[b], 1);
             mbar_init(&acce[b], 4);  // one arrival per epilogue warp
@@ -126,65 +172,79 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_prefetch_desc(&tmX);
     }
     if (warp == 1)
-        tmem_alloc(tmem_slot, a.tmem_cols);
+        tmem_alloc(tmem_slot, 512);  // two accumulators at columns 0 and 256
     tc_fence_before();
     __syncthreads();
-    if (a.cl > 1)
+    if (a.G > 1)
         cluster_sync();  // peers' barriers are initialised before any multicast lands
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------------ producer
-        // W: this CTA's own 128-row tile.  X: the stage's tg token rows;
-        // CTA `rank` fetches `piece` rows starting at min(rank * piece,
-        // tg - piece) and multicasts them to the whole cluster (slices may
-        // overlap at the end; overlapping rows carry identical data and are
-        // counted in the expected bytes).
-        const uint32_t bytes = (uint32_t)(TC_W_BYTES + a.cl * a.piece * TC_BK * 2);
-        const int row0 = min(rank * a.piece, a.tg - a.piece);
+        // W: rows [w0, w0 + wpiece) of the stage's weight tile, multicast
+        // to the cluster (slices may overlap at the end: the overlapping
+        // rows carry identical data and are counted in the expected bytes).
+        // X: this CTA's own n_sub token rows.
+        const uint32_t bytes = (uint32_t)(a.G * a.wpiece * TC_BK * 2 + a.tg * TC_BK * 2);
+        const int w0 = min(rank * a.wpiece, TC_BM - a.wpiece);
+        const SegIter seg_it(u0, u1, a.nkb);
         int it = 0;
         bool ok = true;
-        for (int u = u0; u < u1 && ok; ++u, ++it) {
-            const int qt = u / a.nkb, kb = u % a.nkb;
-            const int mt = (qt / a.n_groups) * a.cl + rank, g = qt % a.n_groups;
-            const int s = it % S;
-            if (it >= S && !mbar_wait(&empty[s], ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, TC_WAIT_NS)) {
-                set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                *abort_flag = 1;
-                ok = false;
-                break;
-            }
-            uint8_t *sw = smem + (size_t)s * stage_bytes;
-            mbar_expect_tx(&full[s], bytes);
-            tma_load_2d(sw, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM);
-            for (int r = row0; r < row0 + a.piece; r += a.box_rows) {
-                uint8_t *dst = sw + TC_W_BYTES + r * TC_BK * 2;
-                if (a.cl > 1)
-                    tma_load_2d_multicast(dst, &tmX, &full[s], kb * TC_BK, g * a.tg + r, mask);
+        for (int i = 0; i < seg_it.n && ok; ++i) {
+            int sa, sb;
+            seg_it.get(i, sa, sb);
+            if (rank == 0)
+                for (int u = sa; u < min(sb, sa + TC_PREFETCH); ++u)
+                    bulk_prefetch_l2(a.w_tiled + (size_t)u * TC_BM * TC_BK, TC_W_BYTES);
+            for (int u = sa; u < sb; ++u, ++it) {
+                const int mt = u / a.nkb, kb = u % a.nkb;
+                const int s = it % S;
+                if (rank == 0 && u + TC_PREFETCH < sb)
+                    bulk_prefetch_l2(a.w_tiled + (size_t)(u + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES);
+                if (it >= S && s % a.rel == 0 &&
+                    !mbar_wait(&empty[s / a.rel], ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, TC_WAIT_NS)) {
+                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                uint8_t *sw = smem + (size_t)s * stage_bytes;
+                mbar_expect_tx(&full[s], bytes);
+                if (a.G > 1)
+                    tma_load_2d_multicast(sw + w0 * TC_BK * 2, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM + w0,
+                                          mask);
                 else
-                    tma_load_2d(dst, &tmX, &full[s], kb * TC_BK, g * a.tg + r);
+                    tma_load_2d(sw, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM);
+                for (int sub = 0; sub < a.nsub; ++sub)
+                    tma_load_2d(sw + TC_W_BYTES + sub * a.n_sub * TC_BK * 2, &tmX, &full[s], kb * TC_BK,
+                                t_base + sub * a.n_sub);
             }
         }
         // tail: wait until every CTA of the cluster released the last use of
-        // each stage, so no arrival or multicast write is still in flight to
-        // this CTA's shared memory when it exits
+        // each stage pair, so no arrival or multicast write is still in
+        // flight to this CTA's shared memory when it exits
         for (int k = (it > S ? it - S : 0); k < it; ++k)
-            mbar_wait(&empty[k % S], (uint32_t)(k / S) & 1u, ok ? abort_flag : nullptr, ok ? TC_WAIT_NS : TC_WAIT_NS / 4);
+            if (k % S % a.rel == 0)
+                mbar_wait(&empty[(k % S) / a.rel], (uint32_t)(k / S) & 1u, ok ? abort_flag : nullptr,
+                          ok ? TC_WAIT_NS : TC_WAIT_NS / 4);
         if (!ok) {
             for (int k = (it > S ? it - S : 0); k < it; ++k)
                 mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u, nullptr, TC_WAIT_NS / 4);
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------------ MMA issuer
+        // A commit costs about as much as four short MMAs, so for N < 224
+        // stages are released in pairs (one commit per two k-blocks).
         const uint32_t idesc = idesc_bf16_f32(TC_BM, a.n_sub);
-        int it = 0, seg = 0;
+        const SegIter seg_it(u0, u1, a.nkb);
+        int it = 0;
         bool ok = true;
-        for (int u = u0; u < u1 && ok; ++seg) {
-            const int kb0 = u % a.nkb;
-            const int kb1 = min(a.nkb, kb0 + (u1 - u));
-            const int buf = seg % a.n_acc;
-            const int use = seg / a.n_acc;
+        for (int seg = 0; seg < seg_it.n && ok; ++seg) {
+            int sa, sb;
+            seg_it.get(seg, sa, sb);
+            const int buf = seg % n_acc;
+            const int use = seg / n_acc;
             if (use > 0 && !mbar_wait(&acce[buf], (uint32_t)(use - 1) & 1u, abort_flag, TC_WAIT_NS)) {
                 set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                 *abort_flag = 1;
@@ -193,7 +253,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d0 = tmem + (uint32_t)(buf * 256);
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            for (int u = sa; u < sb; ++u, ++it) {
                 const int s = it % S;
                 if (!mbar_wait(&full[s], (uint32_t)(it / S) & 1u, abort_flag, TC_WAIT_NS)) {
                     set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
@@ -206,21 +266,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t x_base = w_base + TC_W_BYTES;
                 for (int sub = 0; sub < a.nsub; ++sub) {
 #pragma unroll
-                    for (int k = 0; k < TC_BK / 16; ++k) {
-                        const uint64_t ad = sdesc_kmajor_sw128(w_base + k * 32);
-                        const uint64_t bd = sdesc_kmajor_sw128(x_base + sub * a.n_sub * TC_BK * 2 + k * 32);
-                        mma_bf16(d0 + (uint32_t)(sub * 256), ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < TC_BK / 16; ++k)
+                        mma_bf16(d0 + (uint32_t)(sub * 256), sdesc_kmajor_sw128(w_base + k * 32),
+                                 sdesc_kmajor_sw128(x_base + sub * a.n_sub * TC_BK * 2 + k * 32), idesc,
+                                 (u > sa || k > 0) ? 1u : 0u);
                 }
-                if (a.cl > 1)
-                    mma_commit_multicast(&empty[s], mask);
-                else
-                    mma_commit(&empty[s]);
+                if (s % a.rel == a.rel - 1) {
+                    if (a.G > 1)
+                        mma_commit_multicast(&empty[s / a.rel], mask);
+                    else
+                        mma_commit(&empty[s / a.rel]);
+                }
             }
             if (!ok)
                 break;
             mma_commit(&accf[buf]);
-            u += kb1 - kb0;
+        }
+        if (ok && it % S % a.rel != 0) {
+            // release the partly used last group
+            const int s = (it - 1) % S;
+            if (a.G > 1)
+                mma_commit_multicast(&empty[s / a.rel], mask);
+            else
+                mma_commit(&empty[s / a.rel]);
         }
         if (!ok) {
             mma_commit(drain);
@@ -230,27 +298,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ------------------------------------------------------ epilogue
         // TMEM (thread = output feature, registers = tokens) is transposed
         // through shared memory 32 tokens at a time; each thread then owns
-        // (token, 16 consecutive features) items and applies the fused
-        // epilogue with 16-byte vector accesses.
+        // (token, 16 consecutive features) items.
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int et = threadIdx.x - 64;
         const int row = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        int seg = 0;
-        for (int u = u0; u < u1; ++seg) {
-            const int qt = u / a.nkb, kb0 = u % a.nkb;
-            const int kb1 = min(a.nkb, kb0 + (u1 - u));
-            const int mt = (qt / a.n_groups) * a.cl + rank, g = qt % a.n_groups;
-            const int tile = mt * a.n_groups + g;  // counters
-            const int buf = seg % a.n_acc;
-            const int use = seg / a.n_acc;
+        const bool partial_mode = ep.mode == EPI_PARTIAL;
+        const SegIter seg_it(u0, u1, a.nkb);
+        for (int seg = 0; seg < seg_it.n; ++seg) {
+            int sa, sb;
+            seg_it.get(seg, sa, sb);
+            const int mt = sa / a.nkb, kb0 = sa % a.nkb;
+            const int kb1 = kb0 + (sb - sa);
+            const int tile = mt * a.G + rank;  // arrival counter of this CTA's tile
+            const int buf = seg % n_acc;
+            const int use = seg / n_acc;
             const bool whole = (kb0 == 0 && kb1 == a.nkb);
-            const bool partial_mode = ep.mode == EPI_PARTIAL;
             const bool direct = whole && !partial_mode;
             if (direct && ep.mode == EPI_RESID) {
                 // bring this tile's residual rows into L2 while the MMAs run
                 for (int i = et; i < a.tg * 2; i += 128) {
-                    const int t = g * a.tg + (i >> 1);
+                    const int t = t_base + (i >> 1);
                     if (t < a.T)
                         prefetch_l2(ep.resid + (size_t)t * a.N + mt * TC_BM + (i & 1) * 64);
                 }
@@ -264,50 +332,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
-            const int slot = qt - u0 / a.nkb;
+            const int slot = mt - u0 / a.nkb;
             float *ws_mine = a.ws + ((size_t)cta * a.slots + slot) * a.tg * TC_BM;
-            for (int sub = 0; sub < a.nsub; ++sub) {
-                for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
+            for (int cc = 0; cc < a.nsub * a.n_sub; cc += 32) {
+                const int sub = cc / a.n_sub, c0 = cc % a.n_sub;  // n_sub is a multiple of 32 when nsub == 2
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t r[16];
-                        tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0 + h * 16), r);
-                        tmem_ld_wait();
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0 + h * 16), r);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            stg[(h * 16 + j) * TC_STG_LD + row] = __uint_as_float(r[j]);
-                    }
-                    epi_bar();
+                    for (int j = 0; j < 16; ++j)
+                        stg[(h * 16 + j) * TC_STG_LD + row] = __uint_as_float(r[j]);
+                }
+                epi_bar();
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int it = et + k * 128;
-                        const int j = it >> 3, gq = it & 7;
-                        if (c0 + j < a.n_sub) {
-                            const int col = sub * a.n_sub + c0 + j;
-                            const float4 *sp = reinterpret_cast<const float4 *>(stg + j * TC_STG_LD + gq * 16);
-                            float v[16];
+                for (int k = 0; k < 2; ++k) {
+                    const int it = et + k * 128;
+                    const int j = it >> 3, gq = it & 7;
+                    const int col = sub * a.n_sub + c0 + j;
+                    if (c0 + j < a.n_sub) {
+                        const float4 *sp = reinterpret_cast<const float4 *>(stg + j * TC_STG_LD + gq * 16);
+                        float v[16];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float4 f = sp[e];
-                                v[4 * e] = f.x;
-                                v[4 * e + 1] = f.y;
-                                v[4 * e + 2] = f.z;
-                                v[4 * e + 3] = f.w;
-                            }
-                            if (direct) {
-                                const int t = g * a.tg + col, n0 = mt * TC_BM + gq * 16;
-                                if (t < a.T && n0 < a.N)
-                                    epi_group(ep, t, n0, v);
-                            } else {
-                                float4 *dst = reinterpret_cast<float4 *>(ws_mine + (size_t)col * TC_BM + gq * 16);
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 f = sp[e];
+                            v[4 * e] = f.x;
+                            v[4 * e + 1] = f.y;
+                            v[4 * e + 2] = f.z;
+                            v[4 * e + 3] = f.w;
+                        }
+                        if (direct) {
+                            const int t = t_base + col, n0 = mt * TC_BM + gq * 16;
+                            if (t < a.T && n0 < a.N)
+                                epi_group(ep, t, n0, v);
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(ws_mine + (size_t)col * TC_BM + gq * 16);
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                            }
+                            for (int e = 0; e < 4; ++e)
+                                dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
                         }
                     }
-                    epi_bar();
                 }
+                epi_bar();
             }
             // accumulator buffer free for the MMA warp
             tc_fence_before();
@@ -318,8 +385,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // stream-K fixup: the last contributor to arrive finishes the tile
                 __threadfence();
                 epi_bar();
-                const int c_lo = unit_owner((long long)qt * a.nkb, a);
-                const int c_hi = unit_owner((long long)qt * a.nkb + a.nkb - 1, a);
+                const int c_lo = unit_owner((long long)mt * a.nkb, a);
+                const int c_hi = unit_owner((long long)mt * a.nkb + a.nkb - 1, a);
                 if (et == 0) {
                     const int old = atomicAdd(&a.counters[tile], 1);
                     *last_flag = (old == c_hi - c_lo);
@@ -329,7 +396,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     __threadfence();
                     for (int it = et; it < a.tg * 8; it += 128) {
                         const int col = it >> 3, gq = it & 7;
-                        const int t = g * a.tg + col, n0 = mt * TC_BM + gq * 16;
+                        const int t = t_base + col, n0 = mt * TC_BM + gq * 16;
                         if (t >= a.T || n0 >= a.N)
                             continue;
                         float v[16];
@@ -337,9 +404,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int e = 0; e < 16; ++e)
                             v[e] = 0.f;
                         for (int c = c_lo; c <= c_hi; ++c) {
-                            const int cslot = qt - unit_begin(c, a) / a.nkb;
+                            const int cslot = mt - unit_begin(c, a) / a.nkb;
                             const float4 *src = reinterpret_cast<const float4 *>(
-                                a.ws + (((size_t)(c * a.cl + rank) * a.slots + cslot) * a.tg + col) * TC_BM + gq * 16);
+                                a.ws + (((size_t)(c * a.G + rank) * a.slots + cslot) * a.tg + col) * TC_BM +
+                                gq * 16);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const float4 f = __ldcg(src + e);
@@ -356,16 +424,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 epi_bar();
             }
-            u += kb1 - kb0;
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (a.cl > 1)
+    if (a.G > 1)
         cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, a.tmem_cols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -442,58 +509,44 @@ cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mo
     return cudaGetLastError();
 }
 
-bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K)
+bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, int box_rows)
 {
     const uint64_t npad = (uint64_t)(N + TC_BM - 1) / TC_BM * TC_BM;
     const uint64_t nkb = (uint64_t)(K + TC_BK - 1) / TC_BK;
-    return encode_2d(m, tiled, TC_BK, npad * nkb, TC_BK * 2, TC_BK, TC_BM);
+    return encode_2d(m, tiled, TC_BK, npad * nkb, TC_BK * 2, TC_BK, (uint32_t)box_rows);
 }
 
+int tc_weight_box_rows(int T)
+{
+    const int G = tc_shape(T).G;
+    const int piece = ((TC_BM + G - 1) / G + 7) / 8 * 8;
+    return G > 1 ? piece : TC_BM;
+}
+
+// G = ceil(T / 256) equal token groups of n_sub (a multiple of 16) columns,
+// one MMA of N = n_sub per k-block and two TMEM accumulators per CTA, so
+// the epilogue of one tile overlaps the main loop of the next.  (The kernel
+// also takes two MMAs per k-block, nsub = 2, into one accumulator pair.)
 TcShape tc_shape(int T)
 {
     TcShape sh;
-    if (T <= 256) {
-        sh.nsub = 1;
-        sh.n_sub = (T + 15) / 16 * 16;
-        sh.n_groups = 1;
-    } else if (T <= 512) {
-        sh.nsub = 2;
-        sh.n_sub = ((T + 1) / 2 + 15) / 16 * 16;
-        sh.n_groups = 1;
-    } else {
-        sh.nsub = 1;
-        sh.n_groups = (T + 255) / 256;
-        sh.n_sub = ((T + sh.n_groups - 1) / sh.n_groups + 15) / 16 * 16;
-    }
+    sh.G = (T + 255) / 256;
+    sh.nsub = 1;
+    sh.n_sub = ((T + sh.G - 1) / sh.G + 15) / 16 * 16;
     sh.tg = sh.nsub * sh.n_sub;
     return sh;
 }
 
-// Slots (partial tiles) a CTA can hold: the most tiles any CTA's unit range touches.
+// Slots (partial tiles) a CTA can hold: the most tiles any cluster's unit range touches.
 static int tc_slots(long long units, int grid, int nkb)
 {
     const long long per = (units + grid - 1) / grid;
     return (int)((per + nkb - 1) / nkb + 1);
 }
 
-static int tc_cluster_for(int n_mtiles, int forced)
+static int tc_grid(long long units, int max_clusters)
 {
-    if (forced > 0)
-        return forced;
-    return n_mtiles >= 8 ? 4 : (n_mtiles >= 2 ? 2 : 1);
-}
-
-static void tc_partition_dims(int T, int N, int K, int num_sms, int cl, int &grid, long long &units, int &nkb,
-                              int &tg)
-{
-    const TcShape sh = tc_shape(T);
-    const int n_mtiles = (N + TC_BM - 1) / TC_BM;
-    const int n_quads = (n_mtiles + cl - 1) / cl;
-    nkb = (K + TC_BK - 1) / TC_BK;
-    units = (long long)n_quads * sh.n_groups * nkb;
-    const int max_clusters = num_sms / cl;
-    grid = (int)(units < max_clusters ? units : max_clusters);
-    tg = sh.tg;
+    return (int)(units < max_clusters ? units : max_clusters);
 }
 
 size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes)
@@ -501,55 +554,50 @@ size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int
     size_t need = 0;
     for (int i = 0; i < n_shapes; ++i)
         for (int T = 1; T <= max_tokens; ++T) {
-            for (int cl = 1; cl <= 4; cl *= 2) {
-                int grid, nkb, tg;
-                long long units;
-                tc_partition_dims(T, Ns[i], Ks[i], num_sms, cl, grid, units, nkb, tg);
-                const size_t n = (size_t)grid * cl * tc_slots(units, grid, nkb) * tg * TC_BM;
-                if (n > need)
-                    need = n;
-            }
+            const TcShape sh = tc_shape(T);
+            const int n_mtiles = (Ns[i] + TC_BM - 1) / TC_BM;
+            const int nkb = (Ks[i] + TC_BK - 1) / TC_BK;
+            const long long units = (long long)n_mtiles * nkb;
+            const int grid = tc_grid(units, num_sms / sh.G);
+            const size_t n = (size_t)grid * sh.G * tc_slots(units, grid, nkb) * sh.tg * TC_BM;
+            if (n > need)
+                need = n;
         }
     return need;
 }
 
-cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, int K, const EpiParams &ep,
-                           const TcRuntime &rt, cudaStream_t s, TcPartition *part)
+cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
+                           const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part)
 {
     if (T <= 0)
         return cudaSuccess;
     if (K % 8 != 0)
         return cudaErrorInvalidValue;
     const TcShape sh = tc_shape(T);
+    if (sh.G > TC_MAX_G)
+        return cudaErrorInvalidValue;
     TcArgs a;
     a.T = T;
     a.N = N;
     a.K = K;
     a.n_mtiles = (N + TC_BM - 1) / TC_BM;
     a.nkb = (K + TC_BK - 1) / TC_BK;
-    a.n_groups = sh.n_groups;
-    a.tg = sh.tg;
+    a.G = sh.G;
     a.nsub = sh.nsub;
     a.n_sub = sh.n_sub;
-    a.cl = tc_cluster_for(a.n_mtiles, rt.cluster);
-    a.n_quads = (a.n_mtiles + a.cl - 1) / a.cl;
+    a.tg = sh.tg;
     {
-        int piece = (a.tg + a.cl - 1) / a.cl;
+        int piece = (TC_BM + a.G - 1) / a.G;
         piece = (piece + 7) / 8 * 8;  // whole 1 KB swizzle atoms
-        if (piece < 8)
-            piece = 8;
-        if (piece > a.tg)
-            piece = a.tg;
-        a.piece = piece;
-        a.box_rows = piece <= 256 ? piece : piece / 2;  // tg <= 512, a multiple of 32 when > 256
+        a.wpiece = piece;
     }
-    const long long units = (long long)a.n_quads * a.n_groups * a.nkb;
-    if (units > (1ll << 30) || (long long)a.n_quads * a.cl * a.n_groups > rt.n_counters)
+    const long long units = (long long)a.n_mtiles * a.nkb;
+    if (units > (1ll << 30) || (long long)a.n_mtiles * a.G > rt.n_counters)
         return cudaErrorInvalidValue;
     a.units = (int)units;
     int stages = 10;
     while (stages > 2 && tc_smem_bytes(a.tg, stages) > rt.max_smem)
-        --stages;
+        stages -= 2;  // even: stages are released in pairs
     if (tc_smem_bytes(a.tg, stages) > rt.max_smem)
         return cudaErrorInvalidConfiguration;
     a.stages = stages;
@@ -564,7 +612,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.cl;
+    attr[0].val.clusterDim.x = (unsigned)a.G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(TC_THREADS);
@@ -572,39 +620,39 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // clusters that can be resident at once (cached per cluster size)
-    static int max_clusters[5] = {0, 0, 0, 0, 0};
-    if (!max_clusters[a.cl]) {
-        cfg.gridDim = dim3((unsigned)(rt.num_sms / a.cl * a.cl));
+    // clusters that can be resident at once, cached per (cluster size, stages)
+    static int max_clusters[TC_MAX_G + 1][11] = {};
+    int &mc = max_clusters[a.G][stages];
+    if (!mc) {
+        cfg.gridDim = dim3((unsigned)(rt.num_sms / a.G * a.G));
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess || n <= 0) {
             cudaGetLastError();
-            n = rt.num_sms / a.cl;
+            n = rt.num_sms / a.G;
         }
-        max_clusters[a.cl] = n;
+        mc = n < rt.num_sms / a.G ? n : rt.num_sms / a.G;
     }
-    a.grid = (int)(units < max_clusters[a.cl] ? units : max_clusters[a.cl]);
+    a.grid = tc_grid(units, mc);
     a.slots = tc_slots(units, a.grid, a.nkb);
-    if ((size_t)a.grid * a.cl * a.slots * a.tg * TC_BM > rt.ws_floats)
+    if ((size_t)a.grid * a.G * a.slots * a.tg * TC_BM > rt.ws_floats)
         return cudaErrorInvalidValue;
     if (part) {
         part->ws = rt.ws;
         part->grid = a.grid;
-        part->cl = a.cl;
+        part->G = a.G;
         part->units = a.units;
         part->nkb = a.nkb;
-        part->n_groups = a.n_groups;
         part->tg = a.tg;
         part->slots = a.slots;
     }
-    a.n_acc = (a.nsub == 1) ? 2 : 1;
-    a.tmem_cols = 512;  // two accumulators at columns 0 and 256
     a.ws = rt.ws;
     a.counters = rt.counters;
+    a.w_tiled = W_tiled;
+    a.rel = (a.tg < 224) ? 2 : 1;
     CUtensorMap tmX;
-    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.box_rows))
+    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.n_sub))
         return cudaErrorInvalidValue;
-    cfg.gridDim = dim3((unsigned)(a.grid * a.cl));
+    cfg.gridDim = dim3((unsigned)(a.grid * a.G));
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, tmW, tmX, a, ep);
     if (e != cudaSuccess)
         return e;

@@ -7,10 +7,10 @@
 
 namespace hb {
 
-// Token tiling of a batch of T rows: n_groups groups of tg = nsub * n_sub
-// columns (nsub MMAs of N = n_sub per k-block).
+// Token tiling of a batch of T rows: G groups (one per CTA of a cluster) of
+// tg = nsub * n_sub columns, nsub MMAs of N = n_sub (<= 256) per k-block.
 struct TcShape {
-    int nsub, n_sub, tg, n_groups;
+    int G, nsub, n_sub, tg;
 };
 TcShape tc_shape(int T);
 
@@ -21,18 +21,17 @@ struct TcRuntime {
     size_t ws_floats = 0;
     int *counters = nullptr;  // per-tile arrival counters, zero between launches
     int n_counters = 0;
-    int cluster = 0;          // CTAs per cluster (0: chosen per shape; 1, 2 or 4 forced)
 };
 
-// Where each CTA of one launch left its fp32 partial tiles.  Weight tiles
-// are grouped cl at a time (one cluster); group tile qt = (m_tile / cl) *
-// n_groups + token group covers units [qt*nkb, qt*nkb+nkb) of an even split
-// of `units` over `grid` clusters.  Cluster c's CTA of rank m_tile % cl keeps
-// its share at slot (qt - first group tile of c), element [col][row] of
-// ws + (((c * cl + rank) * slots + slot) * tg) * 128.
+// Where each CTA of one launch left its fp32 partial tiles.  Weight tile mt
+// covers units [mt*nkb, mt*nkb+nkb) of an even split of `units` over `grid`
+// clusters of G CTAs; CTA rank r of a cluster holds token group r (tokens
+// r*tg ..).  Cluster c's rank-r CTA keeps its share of tile mt at slot
+// (mt - first tile of c), element [col][feature % 128] of
+// ws + (((c * G + r) * slots + slot) * tg) * 128.
 struct TcPartition {
     const float *ws = nullptr;
-    int grid = 0, cl = 1, units = 0, nkb = 0, n_groups = 0, tg = 0, slots = 0;
+    int grid = 0, G = 1, units = 0, nkb = 0, tg = 0, slots = 0;
 };
 
 // Workspace floats needed for any batch of up to max_tokens rows and the
@@ -44,16 +43,23 @@ size_t tiled_weight_elems(int N, int K);
 // mode 0: rows as given; 1: RoPE pair permutation within heads of `a` rows;
 // 2: gate/up interleave (gate rows 0..a-1, up rows a..2a-1 of src).
 cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mode, int a, cudaStream_t s);
-bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K);
+// box_rows: 128, or the multicast slice of tc_weight_box_rows(T).
+bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, int box_rows);
+int tc_weight_box_rows(int T);
 
 // acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
 // tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).
-cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *X, int T, int N, int K, const EpiParams &ep,
-                           const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr);
+// W_tiled: the tiled weights tmW describes (streamed into L2 ahead of use).
+cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
+                           const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr);
 
 // out = bf16(resid + sum of the partial tiles of `part`) for T x N outputs;
 // if gamma: norm_out = bf16(out * rsqrt(mean(out^2) + eps) * gamma) per row.
 cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16 *resid, bf16 *out,
                                const float *gamma, bf16 *norm_out, float eps, cudaStream_t s);
+
+// Finish a partial-mode GEMM: sum each (token, 16 stored features) group's
+// partials in cluster order and apply ep's fused epilogue (ep.N % 16 == 0).
+cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s);
 
 }  // namespace hb

@@ -13,8 +13,21 @@ using namespace hb;
 
 namespace hb {
 
+// Tensor maps of a layer's four tiled weights, one per weight-slice height
+// (the slice each CTA of a cluster multicasts depends on the batch's token
+// groups, see tc_weight_box_rows).
+constexpr int kBoxRows[6] = {128, 64, 48, 32, 24, 16};
+enum WKind { W_QKV = 0, W_O, W_GU, W_D };
 struct LayerMaps {
-    CUtensorMap qkv, o, gu, d;
+    CUtensorMap m[4][6];
+    const CUtensorMap &get(int kind, int T) const
+    {
+        const int rows = tc_weight_box_rows(T);
+        int i = 0;
+        while (i < 5 && kBoxRows[i] != rows)
+            ++i;
+        return m[kind][i];
+    }
 };
 
 struct FastPath {
@@ -85,10 +98,13 @@ int hb_init_fast_path(hb_ctx *ctx)
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerDev &L = ctx->layers[l];
         LayerMaps &m = f->maps[l];
-        if (!make_tmap_tiled_weights(&m.qkv, L.w_qkv, ctx->n_qkv, H) ||
-            !make_tmap_tiled_weights(&m.o, L.w_o, H, qd) || !make_tmap_tiled_weights(&m.gu, L.w_gu, ctx->n_gu, H) ||
-            !make_tmap_tiled_weights(&m.d, L.w_d, H, c.ffn))
-            return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
+        for (int i = 0; i < 6; ++i) {
+            if (!make_tmap_tiled_weights(&m.m[W_QKV][i], L.w_qkv, ctx->n_qkv, H, kBoxRows[i]) ||
+                !make_tmap_tiled_weights(&m.m[W_O][i], L.w_o, H, qd, kBoxRows[i]) ||
+                !make_tmap_tiled_weights(&m.m[W_GU][i], L.w_gu, ctx->n_gu, H, kBoxRows[i]) ||
+                !make_tmap_tiled_weights(&m.m[W_D][i], L.w_d, H, c.ffn, kBoxRows[i]))
+                return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
+        }
     }
     ctx->gemm_impl = 1;
     ctx->attn_impl = 1;
@@ -143,16 +159,17 @@ static cudaError_t gemm(hb_ctx *ctx, const CUtensorMap *tmW, const bf16 *X, cons
                         const EpiParams &ep)
 {
     if (ctx->gemm_impl >= 1)
-        return launch_gemm_tc(*tmW, X, T, N, K, ep, ctx->fast->rt, ctx->stream);
+        return launch_gemm_tc(*tmW, W, X, T, N, K, ep, ctx->fast->rt, ctx->stream);
     return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
 }
 
-// One decoder layer.  On the tensor-core path the O-proj and down-proj
-// GEMMs leave split-K partials that one kernel per token finishes together
-// with the residual add and the next RMSNorm (norm-2, and norm-1 of the next
-// layer), so a layer is 7 launches: [norm-1 for the first layer only],
-// QKV GEMM (RoPE + KV append), attention, O GEMM, reduce+residual+norm-2,
-// gate/up GEMM (SwiGLU), down GEMM, reduce+residual(+next norm-1).
+// One decoder layer.  On the tensor-core path the QKV and gate/up GEMMs
+// apply their epilogues (RoPE + KV append, SwiGLU) themselves; the O-proj
+// and down-proj GEMMs leave split-K partials that one kernel per token row
+// finishes with the residual add and the next RMSNorm.  A layer is 7
+// launches: [norm-1 for the first layer only], QKV GEMM, attention, O GEMM,
+// reduce + residual + norm-2, gate/up GEMM, down GEMM, reduce + residual
+// (+ norm-1 of the next layer).
 int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, const bf16 *x, bf16 *y)
 {
     const hb_model_config &c = ctx->cfg;
@@ -182,7 +199,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     ep.v_pool = L.v_pool;
     ep.num_blocks = c.num_blocks;
     ep.err = ctx->err_word;
-    LK(K_GEMM_QKV, gemm(ctx, &M.qkv, ctx->xn, L.w_qkv, T, ctx->n_qkv, H, ep));
+    LK(K_GEMM_QKV, gemm(ctx, &M.get(W_QKV, T), ctx->xn, L.w_qkv, T, ctx->n_qkv, H, ep));
 
     if (ctx->attn_impl == 1) {
         const FastPath *f = ctx->fast;
@@ -222,10 +239,10 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
         pp.T = T;
         pp.N = H;
         TcPartition part;
-        LK(K_GEMM_O, launch_gemm_tc(M.o, ctx->attn_o, T, H, c.n_heads * d, pp, rt, s, &part));
+        LK(K_GEMM_O, launch_gemm_tc(M.get(W_O, T), L.w_o, ctx->attn_o, T, H, c.n_heads * d, pp, rt, s, &part));
         LK(K_REDUCE_NORM, launch_reduce_norm(part, T, H, x, ctx->h, L.g2, ctx->xn, c.rms_eps, s));
-        LK(K_GEMM_GATE_UP, launch_gemm_tc(M.gu, ctx->xn, T, ctx->n_gu, H, eg, rt, s));
-        LK(K_GEMM_DOWN, launch_gemm_tc(M.d, ctx->act, T, H, c.ffn, pp, rt, s, &part));
+        LK(K_GEMM_GATE_UP, launch_gemm_tc(M.get(W_GU, T), L.w_gu, ctx->xn, T, ctx->n_gu, H, eg, rt, s));
+        LK(K_GEMM_DOWN, launch_gemm_tc(M.get(W_D, T), L.w_d, ctx->act, T, H, c.ffn, pp, rt, s, &part));
         const float *g_next = (l + 1 < l_last) ? ctx->layers[l + 1].g1 : nullptr;
         LK(K_REDUCE_NORM, launch_reduce_norm(part, T, H, ctx->h, y, g_next, ctx->xn, c.rms_eps, s));
         return HB_OK;
@@ -237,11 +254,11 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     eo.N = H;
     eo.resid = x;
     eo.out = ctx->h;
-    LK(K_GEMM_O, gemm(ctx, &M.o, ctx->attn_o, L.w_o, T, H, c.n_heads * d, eo));
+    LK(K_GEMM_O, gemm(ctx, &M.get(W_O, T), ctx->attn_o, L.w_o, T, H, c.n_heads * d, eo));
 
     LK(K_RMSNORM, launch_rmsnorm(ctx->h, L.g2, ctx->xn, T, H, c.rms_eps, s));
 
-    LK(K_GEMM_GATE_UP, gemm(ctx, &M.gu, ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
+    LK(K_GEMM_GATE_UP, gemm(ctx, &M.get(W_GU, T), ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
 
     EpiParams ed{};
     ed.mode = EPI_RESID;
@@ -249,7 +266,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     ed.N = H;
     ed.resid = ctx->h;
     ed.out = y;
-    LK(K_GEMM_DOWN, gemm(ctx, &M.d, ctx->act, L.w_d, T, H, c.ffn, ed));
+    LK(K_GEMM_DOWN, gemm(ctx, &M.get(W_D, T), ctx->act, L.w_d, T, H, c.ffn, ed));
     return HB_OK;
 }
 
@@ -282,12 +299,12 @@ extern "C" int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, 
         f->test_w_elems = need;
     }
     CUtensorMap tm;
-    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K))
+    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K, tc_weight_box_rows(T)))
         return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed");
     ctx->n_launches++;
     if (launch_tile_weights((const bf16 *)W, f->test_w, N, K, 0, 0, ctx->stream) != cudaSuccess)
         return ctx->set_error(HB_ECUDA, "tile launch failed");
-    LK(K_GEMM_TEST, launch_gemm_tc(tm, (const bf16 *)X, T, N, K, ep, f->rt, ctx->stream));
+    LK(K_GEMM_TEST, launch_gemm_tc(tm, f->test_w, (const bf16 *)X, T, N, K, ep, f->rt, ctx->stream));
     return HB_OK;
 }
 
@@ -295,11 +312,9 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
 {
     if (!ctx)
         return HB_EINVAL;
-    if (gemm_impl < 0 || gemm_impl > 4 || attn_impl < 0 || attn_impl > 1)
-        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0..4 and attn_impl 0 or 1");
+    if (gemm_impl < 0 || gemm_impl > 1 || attn_impl < 0 || attn_impl > 1)
+        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl and attn_impl must be 0 or 1");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
-    // 1: cluster size chosen per shape; 2, 3, 4: clusters of 1, 2, 4 CTAs
-    ctx->fast->rt.cluster = gemm_impl >= 2 ? (1 << (gemm_impl - 2)) : 0;
     return HB_OK;
 }

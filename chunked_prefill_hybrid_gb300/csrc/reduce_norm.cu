@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
 {
     const int t = blockIdx.x;
     const TcPartition &p = a.part;
-    const int g = t / p.tg, col = t % p.tg;
+    const int r = t / p.tg, col = t % p.tg;
     float h[RN_MAX_GROUPS][8];
     float ss = 0.f;
 #pragma unroll
@@ -43,18 +43,17 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
         const int n0 = (threadIdx.x + i * RN_THREADS) * 8;
         if (n0 >= a.N)
             break;
-        const int mt = n0 >> 7, rank = mt % p.cl;
-        const int qt = (mt / p.cl) * p.n_groups + g;
-        const long long u0 = (long long)qt * p.nkb;
+        const int mt = n0 >> 7;
+        const long long u0 = (long long)mt * p.nkb;
         const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
         float acc[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             acc[k] = 0.f;
         for (int c = c_lo; c <= c_hi; ++c) {
-            const int slot = qt - ubegin(c, p) / p.nkb;
+            const int slot = mt - ubegin(c, p) / p.nkb;
             const float4 *src = reinterpret_cast<const float4 *>(
-                p.ws + ((((size_t)c * p.cl + rank) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
+                p.ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
             const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
             acc[0] += x0.x;
             acc[1] += x0.y;
@@ -103,7 +102,53 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
     }
 }
 
+// Generic finish: every 16-feature group of row t is the sum of its
+// contributors' partials, handed to the fused epilogue (RoPE + KV append
+// for the QKV projection, SwiGLU for gate/up).
+__global__ void __launch_bounds__(128) k_reduce_epi(TcPartition p, EpiParams ep)
+{
+    const int t = blockIdx.x;
+    const int r = t / p.tg, col = t % p.tg;
+    {
+        const int n0 = (blockIdx.y * 128 + threadIdx.x) * 16;
+        if (n0 >= ep.N)
+            return;
+        const int mt = n0 >> 7;
+        const long long u0 = (long long)mt * p.nkb;
+        const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
+        float v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            v[k] = 0.f;
+        for (int c = c_lo; c <= c_hi; ++c) {
+            const int slot = mt - ubegin(c, p) / p.nkb;
+            const float4 *src = reinterpret_cast<const float4 *>(
+                p.ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 f = __ldcg(src + e);
+                v[4 * e] += f.x;
+                v[4 * e + 1] += f.y;
+                v[4 * e + 2] += f.z;
+                v[4 * e + 3] += f.w;
+            }
+        }
+        epi_group(ep, t, n0, v);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s)
+{
+    if (ep.T <= 0)
+        return cudaSuccess;
+    if (ep.N % 16 != 0)
+        return cudaErrorInvalidValue;
+    dim3 grid(ep.T, (ep.N / 16 + 127) / 128);
+    k_reduce_epi<<<grid, 128, 0, s>>>(part, ep);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16 *resid, bf16 *out, const float *gamma,
                                bf16 *norm_out, float eps, cudaStream_t s)

@@ -44,11 +44,13 @@ enum Kind : int {
     K_KVIO,
     K_GEMM_TEST,
     K_REDUCE_NORM,
+    K_REDUCE_QKV,
+    K_REDUCE_SWIGLU,
     K_NUM_KINDS
 };
 static const char *const kKindNames[K_NUM_KINDS] = {"rmsnorm",   "gemm_qkv",  "attention", "attn_combine",
                                                      "gemm_o",    "gemm_gate_up", "gemm_down", "kv_io",
-                                                     "gemm_test", "reduce_norm"};
+                                                     "gemm_test", "reduce_norm", "reduce_qkv", "reduce_swiglu"};
 
 constexpr int kMetaRing = 4;
 
