@@ -553,7 +553,7 @@ size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int
 {
     size_t need = 0;
     for (int i = 0; i < n_shapes; ++i)
-        for (int T = 1; T <= max_tokens; ++T) {
+        for (int T = 1; T <= max_tokens && T <= 2048; ++T) {
             const TcShape sh = tc_shape(T);
             const int n_mtiles = (Ns[i] + TC_BM - 1) / TC_BM;
             const int nkb = (Ks[i] + TC_BK - 1) / TC_BK;

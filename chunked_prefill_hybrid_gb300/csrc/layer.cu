@@ -154,13 +154,73 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
             return ctx->set_error(HB_ECUDA, "launch %s failed: %s", kKindNames[kind], cudaGetErrorString(e_)); \
     } while (0)
 
-// W is in the tiled layout; tmW its tensor map.
-static cudaError_t gemm(hb_ctx *ctx, const CUtensorMap *tmW, const bf16 *X, const bf16 *W, int T, int N, int K,
+// Largest token slab of one tensor-core GEMM launch (8 token groups of 256).
+constexpr int kSlab = 2048;
+
+// The epilogue parameters of rows [t0, t0 + Tn) of a batch.
+static EpiParams epi_rows(const EpiParams &ep, int t0, int Tn)
+{
+    EpiParams e = ep;
+    e.T = Tn;
+    if (e.pos)
+        e.pos += t0;
+    if (e.slot)
+        e.slot += t0;
+    if (e.q_out)
+        e.q_out += (size_t)t0 * e.n_heads * e.head_dim;
+    if (e.resid)
+        e.resid += (size_t)t0 * e.N;
+    if (e.out)
+        e.out += (size_t)t0 * e.N;
+    if (e.act)
+        e.act += (size_t)t0 * e.ffn;
+    if (e.d32)
+        e.d32 += (size_t)t0 * e.N;
+    return e;
+}
+
+// W is in the tiled layout; tmW its tensor map (for a slab of kSlab rows
+// when T is larger: the weight slice height depends on the slab's rows).
+static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X, const bf16 *W, int T, int N, int K,
                         const EpiParams &ep)
 {
-    if (ctx->gemm_impl >= 1)
-        return launch_gemm_tc(*tmW, W, X, T, N, K, ep, ctx->fast->rt, ctx->stream);
-    return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
+    if (ctx->gemm_impl == 0)
+        return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
+    ctx->n_launches += (T + kSlab - 1) / kSlab - 1;  // one is counted by the caller
+    for (int t0 = 0; t0 < T; t0 += kSlab) {
+        const int Tn = T - t0 < kSlab ? T - t0 : kSlab;
+        cudaError_t e = launch_gemm_tc(M.get(kind, Tn), W, X + (size_t)t0 * K, Tn, N, K, epi_rows(ep, t0, Tn),
+                                       ctx->fast->rt, ctx->stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+// Tensor-core GEMM leaving partials, then the fused reduce + residual (+ norm),
+// slab by slab.
+static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X, const bf16 *W, int T, int N,
+                               int K, const bf16 *resid, bf16 *out, const float *gamma, bf16 *norm_out, int *launches)
+{
+    const hb_model_config &c = ctx->cfg;
+    for (int t0 = 0; t0 < T; t0 += kSlab) {
+        const int Tn = T - t0 < kSlab ? T - t0 : kSlab;
+        EpiParams pp{};
+        pp.mode = EPI_PARTIAL;
+        pp.T = Tn;
+        pp.N = N;
+        TcPartition part;
+        cudaError_t e = launch_gemm_tc(M.get(kind, Tn), W, X + (size_t)t0 * K, Tn, N, K, pp, ctx->fast->rt,
+                                       ctx->stream, &part);
+        if (e != cudaSuccess)
+            return e;
+        e = launch_reduce_norm(part, Tn, N, resid + (size_t)t0 * N, out + (size_t)t0 * N, gamma,
+                               norm_out + (size_t)t0 * N, c.rms_eps, ctx->stream);
+        if (e != cudaSuccess)
+            return e;
+        *launches += 2;
+    }
+    return cudaSuccess;
 }
 
 // One decoder layer.  On the tensor-core path the QKV and gate/up GEMMs
@@ -199,7 +259,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     ep.v_pool = L.v_pool;
     ep.num_blocks = c.num_blocks;
     ep.err = ctx->err_word;
-    LK(K_GEMM_QKV, gemm(ctx, &M.get(W_QKV, T), ctx->xn, L.w_qkv, T, ctx->n_qkv, H, ep));
+    LK(K_GEMM_QKV, gemm(ctx, M, W_QKV, ctx->xn, L.w_qkv, T, ctx->n_qkv, H, ep));
 
     if (ctx->attn_impl == 1) {
         const FastPath *f = ctx->fast;
@@ -233,18 +293,14 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     eg.ffn = c.ffn;
 
     if (tc) {
-        const TcRuntime &rt = ctx->fast->rt;
-        EpiParams pp{};
-        pp.mode = EPI_PARTIAL;
-        pp.T = T;
-        pp.N = H;
-        TcPartition part;
-        LK(K_GEMM_O, launch_gemm_tc(M.get(W_O, T), L.w_o, ctx->attn_o, T, H, c.n_heads * d, pp, rt, s, &part));
-        LK(K_REDUCE_NORM, launch_reduce_norm(part, T, H, x, ctx->h, L.g2, ctx->xn, c.rms_eps, s));
-        LK(K_GEMM_GATE_UP, launch_gemm_tc(M.get(W_GU, T), L.w_gu, ctx->xn, T, ctx->n_gu, H, eg, rt, s));
-        LK(K_GEMM_DOWN, launch_gemm_tc(M.get(W_D, T), L.w_d, ctx->act, T, H, c.ffn, pp, rt, s, &part));
+        // launch counting: LK counts one launch per call; gemm_reduce reports its own
+        int extra = 0;
+        LK(K_GEMM_O, gemm_reduce(ctx, M, W_O, ctx->attn_o, L.w_o, T, H, c.n_heads * d, x, ctx->h, L.g2, ctx->xn,
+                                 &extra));
+        LK(K_GEMM_GATE_UP, gemm(ctx, M, W_GU, ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
         const float *g_next = (l + 1 < l_last) ? ctx->layers[l + 1].g1 : nullptr;
-        LK(K_REDUCE_NORM, launch_reduce_norm(part, T, H, ctx->h, y, g_next, ctx->xn, c.rms_eps, s));
+        LK(K_GEMM_DOWN, gemm_reduce(ctx, M, W_D, ctx->act, L.w_d, T, H, c.ffn, ctx->h, y, g_next, ctx->xn, &extra));
+        ctx->n_launches += extra - 2;
         return HB_OK;
     }
 
@@ -254,11 +310,11 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     eo.N = H;
     eo.resid = x;
     eo.out = ctx->h;
-    LK(K_GEMM_O, gemm(ctx, &M.get(W_O, T), ctx->attn_o, L.w_o, T, H, c.n_heads * d, eo));
+    LK(K_GEMM_O, gemm(ctx, M, W_O, ctx->attn_o, L.w_o, T, H, c.n_heads * d, eo));
 
     LK(K_RMSNORM, launch_rmsnorm(ctx->h, L.g2, ctx->xn, T, H, c.rms_eps, s));
 
-    LK(K_GEMM_GATE_UP, gemm(ctx, &M.get(W_GU, T), ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
+    LK(K_GEMM_GATE_UP, gemm(ctx, M, W_GU, ctx->xn, L.w_gu, T, ctx->n_gu, H, eg));
 
     EpiParams ed{};
     ed.mode = EPI_RESID;
@@ -266,7 +322,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     ed.N = H;
     ed.resid = ctx->h;
     ed.out = y;
-    LK(K_GEMM_DOWN, gemm(ctx, &M.get(W_D, T), ctx->act, L.w_d, T, H, c.ffn, ed));
+    LK(K_GEMM_DOWN, gemm(ctx, M, W_D, ctx->act, L.w_d, T, H, c.ffn, ed));
     return HB_OK;
 }
 

@@ -184,6 +184,10 @@ class Context:
             self._check(self.L.hb_forward_layers(self.h, ctypes.byref(spec.c), layers[0], layers[1], _ptr(x_in),
                                                  _ptr(x_out)))
 
+    def forward_spec(self, spec: "BatchSpec", x_in, x_out):
+        """Forward with a raw BatchSpec (e.g. one the scheduler filled)."""
+        self._check(self.L.hb_forward(self.h, ctypes.byref(spec), _ptr(x_in), _ptr(x_out)))
+
     def forward_host(self, spec: Spec, x_in: np.ndarray, x_out: np.ndarray):
         assert x_in.flags.c_contiguous and x_out.flags.c_contiguous
         self._check(self.L.hb_forward_host(self.h, ctypes.byref(spec.c), x_in.ctypes.data, x_out.ctypes.data))

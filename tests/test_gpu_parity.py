@@ -139,7 +139,7 @@ def test_tiny_gamma_uniform_and_multilayer():
     w = _tiny(12, 40, 50, [10, 70, 130], n_layers=3, gamma="uniform")
     ctx, y = run_gpu(w)
     ref, pools = oracle_run(w)
-    ok, st = compare(y, ref)
+    ok, st = compare(y, ref, layers=3)
     assert ok, st
     for l in range(3):
         check_kv(ctx, w, pools, layer=l)
@@ -211,6 +211,66 @@ def test_llama13b_hybrid_full_layer():
     """LLaMA-13B layer, chunk 256 at offset 768 + 18 decodes at ctx 1024 (T = 274): every row."""
     w = workloads.llama13b_hybrid(seed=2)
     ctx, y = run_gpu(w, poison=True)
+    ref, pools = oracle_run(w)
+    ok, st = compare(y, ref)
+    assert ok, st
+    ctx.free()
+
+
+def test_llama13b_three_layers_sampled_rows():
+    """Three LLaMA-13B layers, chunk 256 @ 768 + 12 decodes with ctx in [128, 2048]: the first 16 chunk
+    rows (causally closed) and every decode row through all layers against the oracle."""
+    ctxs = synth.uniform_ints(3, (9,), 12, 128, 2048)
+    w = workloads.make("13b-3layer", synth.LLAMA_13B, 3, 768, 256, ctxs, n_layers=3)
+    ctx, y = run_gpu(w)
+    rows = np.zeros(w.T, bool)
+    rows[:16] = True
+    rows[w.batch.chunk_len:] = True
+    ref, pools = oracle_run(w, rows=rows)
+    ok, st = compare(y[rows], ref[rows], layers=3)
+    assert ok, st
+    ctx.free()
+
+
+@pytest.mark.parametrize("C", [255, 256, 257, 1024])
+def test_long_context_chunked_equals_monolithic(C):
+    """Long prompts (log-uniform up to ~6000 tokens) as chunks of C on the GPU equal the oracle's monolithic
+    prefill, with shuffled block tables and decodes at long contexts piggybacked (head_dim 128, 2 layers)."""
+    seed = 17
+    dims = D128.with_layers(2)
+    P = int(synth.log_uniform_ints(seed, (C,), 1, 512, 6000)[0])
+    dec_ctx = [int(c) for c in synth.log_uniform_ints(seed, (C, 2), 3, 256, 8000)]
+    w = workloads.make("long", dims, seed, 0, P, dec_ctx, n_layers=2)
+    cfg = workloads.config(w, max_tokens=max(P, C) + len(dec_ctx), max_decodes=len(dec_ctx))
+    ctx = native.Context(cfg)
+    workloads.upload(w, ctx)
+    # chunked on the GPU: the decodes ride on the first chunk only
+    out = np.zeros((P, dims.hidden))
+    for s0 in range(0, P, C):
+        ln = min(C, P - s0)
+        decs = w.batch.decodes if s0 == 0 else []
+        b = synth.HybridBatch(synth.Seq(0, s0, w.batch.chunk.block_table), ln, decs)
+        xin = np.concatenate([w.x[s0:s0 + ln]] + ([w.x[P:]] if decs else []))
+        xd = workloads.to_device(xin)
+        yd = torch.empty_like(xd)
+        ctx.forward(native.Spec(b), xd, yd)
+        ctx.sync()
+        yy = f64(_bits(yd))
+        out[s0:s0 + ln] = yy[:ln]
+        if decs:
+            dec_out = yy[ln:]
+    ref, _ = oracle_run(w)          # the whole prompt as one monolithic chunk + the decodes
+    ok, st = compare(out, ref[:P], layers=2)
+    assert ok, (C, P, st)
+    ok, st = compare(dec_out, ref[P:], layers=2)
+    assert ok, (C, st)
+    ctx.free()
+
+
+def test_monolithic_prefill_larger_than_one_gemm_slab():
+    """A 2300-row prefill (more than one 2048-row GEMM launch) against the oracle."""
+    w = _tiny(18, 0, 2300, [5, 700])
+    ctx, y = run_gpu(w)
     ref, pools = oracle_run(w)
     ok, st = compare(y, ref)
     assert ok, st
