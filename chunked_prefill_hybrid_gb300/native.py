@@ -25,7 +25,8 @@ _NAMES = {0: "HB_OK", -1: "HB_EINVAL", -2: "HB_ERANGE", -3: "HB_ENOMEM", -4: "HB
 # Every symbol include/hb.h declares.
 ABI_SYMBOLS = ["hb_init", "hb_load_layer", "hb_append_kv", "hb_read_kv", "hb_fill_kv", "hb_forward",
                "hb_forward_layers", "hb_forward_host", "hb_sync", "hb_profile", "hb_profile_read",
-               "hb_launch_count", "hb_gemm_test", "hb_debug_read", "hb_set_kernels", "hb_plan", "hb_last_error", "hb_free"]
+               "hb_launch_count", "hb_gemm_test", "hb_debug_read", "hb_set_kernels", "hb_plan", "hb_last_error", "hb_free",
+               "hb_decode_attention_noalloc"]
 
 
 class HbError(RuntimeError):
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
         "hb_plan": ([P(ModelConfig), P(BatchSpec), vp, vp, ctypes.c_char_p, ci], ci),
         "hb_last_error": ([vp], ctypes.c_char_p),
         "hb_free": ([vp], None),
+        "hb_decode_attention_noalloc": ([vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp], ci),
     }
     for name, (args, res) in sig.items():
         f = getattr(L, name)
@@ -139,6 +141,25 @@ def plan(cfg: ModelConfig, spec: Spec):
 
 def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
+
+
+def decode_attention_noalloc(q, k_pool, v_pool, block_tables, ctx_lens, max_ctx: int, out, stream=None):
+    """hb_decode_attention_noalloc on device tensors (no context, no device
+    allocation): q, out [n][n_heads][head_dim] bf16 (as int16/uint16/bf16
+    storage); k_pool, v_pool [num_blocks][n_kv][16][head_dim]; block_tables
+    int32 [n][stride]; ctx_lens int32 [n].  Raises HbError on a bad call."""
+    import torch
+    n, n_heads, head_dim = q.shape
+    num_blocks, n_kv = k_pool.shape[0], k_pool.shape[1]
+    for t in (q, k_pool, v_pool, block_tables, ctx_lens, out):
+        if not t.is_contiguous():
+            raise ValueError("decode_attention_noalloc wants contiguous tensors")
+    st = stream if stream is not None else torch.cuda.current_stream()
+    rc = lib().hb_decode_attention_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                           int(block_tables.shape[1]), _ptr(ctx_lens), n, n_heads, n_kv, head_dim,
+                                           num_blocks, int(max_ctx), _ptr(out), ctypes.c_void_p(st.cuda_stream))
+    if rc:
+        raise HbError(rc, "hb_decode_attention_noalloc failed")
 
 
 class Context:

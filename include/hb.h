@@ -196,6 +196,43 @@ int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl);
  * Valid after hb_sync.  rows: the batch's T. */
 int hb_debug_read(hb_ctx *ctx, int which, void *dst, int rows);
 
+/* Paged decode attention that allocates no device memory.
+ *
+ * This call has no counterpart on the pages: it is a library convenience
+ * for callers that must not allocate -- an engine that has handed nearly
+ * all HBM to its own KV-cache arena, or code that may not call
+ * cudaMalloc / cudaFree (they can stall every stream on the device) while
+ * other work runs.  It needs no hb_ctx.
+ *
+ * Computes what the batch forward's attention computes for decode rows:
+ * query j at position ctx_lens[j] attends keys 0..ctx_lens[j] of its own
+ * sequence, found through its block table, softmax(q k^T / sqrt(head_dim)) v,
+ * with grouped-query heads (head h reads kv head h / (n_heads / n_kv_heads)).
+ *   q, out:       device bf16 [n_decodes][n_heads][head_dim]
+ *   k_pool, v_pool: device bf16 [num_blocks][n_kv_heads][16][head_dim]
+ *   block_tables: device int32 [n_decodes][bt_stride], bt_stride >=
+ *                 max_ctx / 16 + 1
+ *   ctx_lens:     device int32 [n_decodes], each in [0, max_ctx]
+ *   head_dim 64 or 128; cuda_stream: a cudaStream_t, NULL = legacy default.
+ * Split partials and arrival counters live in one fixed static device array
+ * inside the library (about 8.5 MB), which bounds the call:
+ *   n_decodes * n_heads <= 4096 and
+ *   n_decodes * n_heads * ceil((max_ctx + 1) / 256) <= 16384;
+ * larger calls return HB_ERANGE and launch nothing.  Other errors:
+ * HB_EINVAL (bad argument), HB_ECUDA (a CUDA call failed).  A row whose
+ * ctx_lens entry lies outside [0, max_ctx], or whose table holds a block id
+ * outside [0, num_blocks), gets NaN.
+ * The first call on each device (with that device current) looks up the
+ * array's device address and zeroes its counters on cuda_stream; make that
+ * first call before any stream capture.  Every call leaves the counters at
+ * zero.  All calls on a device share the array, so calls that can overlap
+ * on the GPU (different streams without ordering) race and give wrong
+ * results: order them.  Asynchronous; errors of the kernel itself show as
+ * NaN rows, not as a return code. */
+int hb_decode_attention_noalloc(const void *q, const void *k_pool, const void *v_pool, const int32_t *block_tables,
+                                int bt_stride, const int32_t *ctx_lens, int n_decodes, int n_heads, int n_kv_heads,
+                                int head_dim, int num_blocks, int max_ctx, void *out, void *cuda_stream);
+
 /* Host-only planning of one batch (no GPU, no context needed): validates
  * spec against cfg exactly as hb_forward does and writes each row's
  * absolute position and physical KV slot.  pos, slot: host int32 [T] or
