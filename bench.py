@@ -263,6 +263,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", action="store_true",
+                    help="run only the warm-up and --steps hybrid steps, untimed (the case ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -298,6 +300,13 @@ def main():
     for _ in range(args.warmup):
         step()
     ctx.sync()
+    if args.ncu_case:
+        for _ in range(args.steps):
+            step()
+        ctx.sync()
+        ctx.free()
+        print(f"ncu case: {args.warmup} + {args.steps} steps of {WORKLOAD}", flush=True)
+        return 0
 
     # 1) the headline: hybrid batch, inputs resident
     n0 = ctx.launch_count

@@ -133,11 +133,32 @@ __device__ __forceinline__ uint4 pack8_bf16(const float (&x)[8])
     return u;
 }
 
+// RoPE (cos, sin) of the 8 rotate-half pairs held by the 16 stored QKV
+// features n0..n0+15 at position pos (identity outside the q and k heads).
+__device__ __forceinline__ void qkv_rope_load(const EpiParams &p, int pos, int n0, float4 (&cs)[4])
+{
+    const int d = p.head_dim, half = d >> 1;
+    const int hb = n0 / d, i0 = (n0 % d) >> 1;
+    if (hb < p.n_heads + p.n_kv) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.rope + (size_t)pos * half + i0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            cs[k] = __ldg(src + k);  // (cos, sin) of pairs 2k and 2k+1
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            cs[k] = make_float4(1.f, 0.f, 1.f, 0.f);
+    }
+}
+
 // The same epilogue as epi_pair over 16 consecutive stored output features
 // n0..n0+15 (n0 % 16 == 0) of token t, with 16-byte vector memory accesses.
 // For EPI_QKV the 16 stored rows are 8 RoPE pairs: head features i0..i0+7
-// and i0+d/2..i0+d/2+7; for EPI_SWIGLU they are 8 (gate, up) pairs.
-__device__ __forceinline__ void epi_group(const EpiParams &p, int t, int n0, const float (&v)[16])
+// and i0+d/2..i0+d/2+7, rotated by cs (from qkv_rope_load at the row's
+// position) and written to q or to the row's KV slot; for EPI_SWIGLU they
+// are 8 (gate, up) pairs.
+__device__ __forceinline__ void epi_group_at(const EpiParams &p, int t, int n0, const float (&v)[16], int slot_t,
+                                             const float4 (&cs)[4])
 {
     switch (p.mode) {
     case EPI_F32: {
@@ -164,10 +185,9 @@ __device__ __forceinline__ void epi_group(const EpiParams &p, int t, int n0, con
             hi[k] = v[2 * k + 1];
         }
         if (hb < p.n_heads + p.n_kv) {
-            const float4 *cs = reinterpret_cast<const float4 *>(p.rope + (size_t)p.pos[t] * half + i0);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 c = cs[k];  // (cos, sin) of pairs 2k and 2k+1
+                const float4 c = cs[k];
                 const float x0 = lo[2 * k], x1 = hi[2 * k], y0 = lo[2 * k + 1], y1 = hi[2 * k + 1];
                 lo[2 * k] = x0 * c.x - x1 * c.y;
                 hi[2 * k] = x1 * c.x + x0 * c.y;
@@ -179,8 +199,7 @@ __device__ __forceinline__ void epi_group(const EpiParams &p, int t, int n0, con
         if (hb < p.n_heads) {
             base = p.q_out + (size_t)t * p.n_heads * d + (size_t)hb * d;
         } else {
-            const int s = p.slot[t];
-            const int blk = s >> 4, off = s & 15;
+            const int blk = slot_t >> 4, off = slot_t & 15;
             if (blk < 0 || blk >= p.num_blocks) {
                 set_dev_err(p.err, DERR_BAD_SLOT);
                 return;
@@ -221,6 +240,18 @@ __device__ __forceinline__ void epi_group(const EpiParams &p, int t, int n0, con
         break;
     }
     }
+}
+
+// epi_group_at with the row's position and slot read from p.pos / p.slot.
+__device__ __forceinline__ void epi_group(const EpiParams &p, int t, int n0, const float (&v)[16])
+{
+    float4 cs[4];
+    int slot_t = 0;
+    if (p.mode == EPI_QKV) {
+        qkv_rope_load(p, p.pos[t], n0, cs);
+        slot_t = p.slot[t];
+    }
+    epi_group_at(p, t, n0, v, slot_t, cs);
 }
 
 }  // namespace hb

@@ -59,6 +59,7 @@ struct TcArgs {
     int nsub;         // MMAs per k-block (1 or 2; the second accumulates at TMEM column 256)
     int n_sub;        // tokens per MMA (multiple of 16, <= 256); a CTA holds tg = nsub * n_sub
     int tg;
+    int n_sub32;      // n_sub rounded up to 32 (the epilogue's column chunks)
     int wpiece;       // weight-tile rows each CTA fetches and multicasts
     int units, grid;  // units = n_mtiles * nkb over `grid` clusters
     int stages, slots;
@@ -106,14 +107,18 @@ struct SegIter {
     }
 };
 
-// Epilogue staging tile: 32 token columns x 128 features, fp32, padded rows.
-constexpr int TC_STG_LD = 132;
-constexpr int TC_STG_BYTES = 32 * TC_STG_LD * 4;
+// Epilogue shared memory: position and KV slot of each of the CTA's token
+// columns (at most 2 x 256), read by the fused QKV epilogue, and one
+// 32 x 32 transpose tile per epilogue warp (rows padded to 33 floats).
+constexpr int TC_MAX_TG = 512;
+constexpr int TC_META_BYTES = 2 * TC_MAX_TG * 4;
+constexpr int TC_XP_LD = 33;
+constexpr int TC_XP_BYTES = 4 * 32 * TC_XP_LD * 4;
 
 __host__ __device__ inline int tc_stage_bytes(int tg) { return TC_W_BYTES + tg * TC_BK * 2; }
 __host__ __device__ inline int tc_smem_bytes(int tg, int stages)
 {
-    return stages * tc_stage_bytes(tg) + 256 + TC_STG_BYTES + 1024;
+    return stages * tc_stage_bytes(tg) + 256 + TC_META_BYTES + TC_XP_BYTES + 1024;
 }
 
 __device__ __forceinline__ int unit_owner(long long u, const TcArgs &a)
@@ -128,6 +133,112 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Fused epilogue of ncol (<= 32) token columns col0.. of this CTA for the
+// warp's 32 features nb..nb+31 (lane = feature); r holds the fp32
+// accumulator bits, one token column per register.  Every lane of the warp
+// calls this together.
+//   EPI_F32: one coalesced 128-byte store per token.
+//   bf16 outputs (EPI_QKV, EPI_SWIGLU, EPI_RESID): the warp transposes its
+//   32 x 32 block through its own shared-memory tile so that a lane owns
+//   (token, 16 consecutive features) items, which epi_group_at writes with
+//   16-byte stores; the QKV rotation tables of both items are loaded before
+//   either item is stored.
+__device__ __forceinline__ void emit_cols(const EpiParams &p, const int *s_pos, const int *s_slot, float *xp,
+                                          int t_base, int col0, int ncol, int nb, int lane, const uint32_t (&r)[32])
+{
+    if (p.mode == EPI_F32) {
+        const int n = nb + lane;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = t_base + col0 + j;
+            if (j < ncol && t < p.T && n < p.N)
+                p.d32[(size_t)t * p.N + n] = __uint_as_float(r[j]);
+        }
+        return;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        xp[j * TC_XP_LD + lane] = __uint_as_float(r[j]);  // row = token, column = feature
+    __syncwarp();
+    const int g = lane & 1;
+    const int n0 = nb + g * 16;
+    float v[2][16];
+    float4 cs[2][4];
+    int c[2];
+    bool ok[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int j = (lane >> 1) + 16 * k;
+        c[k] = col0 + j;
+        ok[k] = j < ncol && t_base + c[k] < p.T && n0 < p.N;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            v[k][e] = xp[j * TC_XP_LD + g * 16 + e];
+        if (p.mode == EPI_QKV && ok[k])
+            qkv_rope_load(p, s_pos[c[k]], n0, cs[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        if (ok[k])
+            epi_group_at(p, t_base + c[k], n0, v[k], p.mode == EPI_QKV ? s_slot[c[k]] : 0, cs[k]);
+}
+
+// Stream-K fixup of one tile by its last contributor: the sum of every
+// contributor's fp32 partial, added in contributor order so the result does
+// not depend on timing, then the fused epilogue.  Warp q covers the
+// features nb.. of its quadrant for all the CTA's token columns; each
+// contributor's row of 32 features is one coalesced 128-byte load.
+__device__ __forceinline__ void fixup_tile(const EpiParams &ep, const TcArgs &a, const int *s_pos, const int *s_slot,
+                                           float *xp, int rank, int t_base, int mt, int c_lo, int c_hi, int nb, int f,
+                                           int lane)
+{
+    constexpr int MAXC = 8;  // contributors whose partials are loaded together
+    const int ncon = c_hi - c_lo + 1;
+    const float *src[MAXC];
+#pragma unroll
+    for (int k = 0; k < MAXC; ++k) {
+        const int c = c_lo + min(k, ncon - 1);
+        const int cslot = mt - unit_begin(c, a) / a.nkb;
+        src[k] = a.ws + ((size_t)(c * a.G + rank) * a.slots + cslot) * a.tg * TC_BM + f;
+    }
+    for (int c0 = 0; c0 < a.tg; c0 += 32) {
+        const int ncol = min(32, a.tg - c0);
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            acc[j] = 0.f;
+        for (int cb = 0; cb < ncon; cb += MAXC) {
+            if (ncon > MAXC) {
+                // tiles split over more than MAXC clusters: this group's partials
+#pragma unroll
+                for (int k = 0; k < MAXC; ++k) {
+                    const int c = c_lo + min(cb + k, ncon - 1);
+                    const int cslot = mt - unit_begin(c, a) / a.nkb;
+                    src[k] = a.ws + ((size_t)(c * a.G + rank) * a.slots + cslot) * a.tg * TC_BM + f;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < MAXC; ++k) {
+                if (cb + k < ncon) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = j < ncol ? __ldcg(src[k] + (size_t)(c0 + j) * TC_BM) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[j] += v[j];
+                }
+            }
+        }
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            r[j] = __float_as_uint(acc[j]);
+        emit_cols(ep, s_pos, s_slot, xp, t_base, c0, ncol, nb, lane, r);
+    }
+}
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
@@ -145,7 +256,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint32_t *tmem_slot = (uint32_t *)(drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
-    float *stg = (float *)(smem + (size_t)S * stage_bytes + 256);  // [32][TC_STG_LD]
+    int *s_pos = (int *)(smem + (size_t)S * stage_bytes + 256);  // [TC_MAX_TG]
+    int *s_slot = s_pos + TC_MAX_TG;                               // [TC_MAX_TG]
+    float *s_xp = (float *)(s_slot + TC_MAX_TG);                   // [4][32][TC_XP_LD]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = a.G > 1 ? (int)cluster_ctarank() : 0;  // token group of this CTA
@@ -171,6 +284,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
     }
+    if (ep.mode == EPI_QKV)
+        for (int c = threadIdx.x; c < a.tg; c += TC_THREADS) {
+            const int t = t_base + c;
+            s_pos[c] = t < a.T ? ep.pos[t] : 0;
+            s_slot[c] = t < a.T ? ep.slot[t] : -1;
+        }
     if (warp == 1)
         tmem_alloc(tmem_slot, 512);  // two accumulators at columns 0 and 256
     tc_fence_before();
@@ -180,45 +299,60 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
+    // Ring position: stage s of S, lap parity ph; stages are released in
+    // groups of rel (1 or 2) consecutive stages.  Kept as counters so the
+    // single-warp loops below do no integer division.
+    const int rel_mask = a.rel - 1, rel_shift = a.rel == 2 ? 1 : 0;
+    if (warp == 0) {
         // ------------------------------------------------------ producer
+        // The whole warp runs this loop (warp-uniform values); one elected
+        // lane issues each copy.
         // W: rows [w0, w0 + wpiece) of the stage's weight tile, multicast
         // to the cluster (slices may overlap at the end: the overlapping
         // rows carry identical data and are counted in the expected bytes).
-        // X: this CTA's own n_sub token rows.
+        // X: this CTA's own token rows, nsub boxes of n_sub.
         const uint32_t bytes = (uint32_t)(a.G * a.wpiece * TC_BK * 2 + a.tg * TC_BK * 2);
         const int w0 = min(rank * a.wpiece, TC_BM - a.wpiece);
         const SegIter seg_it(u0, u1, a.nkb);
-        int it = 0;
+        int it = 0, s = 0;
+        uint32_t ph = 0;
         bool ok = true;
         for (int i = 0; i < seg_it.n && ok; ++i) {
             int sa, sb;
             seg_it.get(i, sa, sb);
             if (rank == 0)
                 for (int u = sa; u < min(sb, sa + TC_PREFETCH); ++u)
-                    bulk_prefetch_l2(a.w_tiled + (size_t)u * TC_BM * TC_BK, TC_W_BYTES);
-            for (int u = sa; u < sb; ++u, ++it) {
-                const int mt = u / a.nkb, kb = u % a.nkb;
-                const int s = it % S;
+                    bulk_prefetch_l2_elect(a.w_tiled + (size_t)u * TC_BM * TC_BK, TC_W_BYTES);
+            const int mt = sa / a.nkb;  // a segment lies within one weight tile
+            int w_row = sa * TC_BM + w0;  // row of the tiled weights: (mt * nkb + kb) * 128 + w0
+            int kx = (sa - mt * a.nkb) * TC_BK;
+            for (int u = sa; u < sb; ++u, ++it, w_row += TC_BM, kx += TC_BK) {
                 if (rank == 0 && u + TC_PREFETCH < sb)
-                    bulk_prefetch_l2(a.w_tiled + (size_t)(u + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES);
-                if (it >= S && s % a.rel == 0 &&
-                    !mbar_wait(&empty[s / a.rel], ((uint32_t)(it / S) & 1u) ^ 1u, abort_flag, TC_WAIT_NS)) {
-                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                    *abort_flag = 1;
+                    bulk_prefetch_l2_elect(a.w_tiled + (size_t)(u + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES);
+                if (it >= S && (s & rel_mask) == 0 &&
+                    !__all_sync(0xffffffffu, mbar_wait(&empty[s >> rel_shift], ph ^ 1u, abort_flag, TC_WAIT_NS))) {
+                    if (lane == 0) {
+                        set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
                     ok = false;
                     break;
                 }
                 uint8_t *sw = smem + (size_t)s * stage_bytes;
-                mbar_expect_tx(&full[s], bytes);
+                mbar_expect_tx_elect(&full[s], bytes);
                 if (a.G > 1)
-                    tma_load_2d_multicast(sw + w0 * TC_BK * 2, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM + w0,
-                                          mask);
+                    tma_load_2d_multicast_elect(sw + w0 * TC_BK * 2, &tmW, &full[s], 0, w_row, mask);
                 else
-                    tma_load_2d(sw, &tmW, &full[s], 0, (mt * a.nkb + kb) * TC_BM);
-                for (int sub = 0; sub < a.nsub; ++sub)
-                    tma_load_2d(sw + TC_W_BYTES + sub * a.n_sub * TC_BK * 2, &tmX, &full[s], kb * TC_BK,
-                                t_base + sub * a.n_sub);
+                    tma_load_2d_elect(sw, &tmW, &full[s], 0, w_row);
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub)
+                    if (sub < a.nsub)
+                        tma_load_2d_elect(sw + TC_W_BYTES + sub * a.n_sub * TC_BK * 2, &tmX, &full[s], kx,
+                                          t_base + sub * a.n_sub);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
         }
         // tail: wait until every CTA of the cluster released the last use of
@@ -232,76 +366,99 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int k = (it > S ? it - S : 0); k < it; ++k)
                 mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u, nullptr, TC_WAIT_NS / 4);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        // A commit costs about as much as four short MMAs, so for N < 224
-        // stages are released in pairs (one commit per two k-blocks).
+        // The whole warp runs this loop; one elected lane issues each MMA
+        // and commit.  A commit costs about as much as four short MMAs, so
+        // for N < 224 stages are released in pairs (one commit per two
+        // k-blocks).
         const uint32_t idesc = idesc_bf16_f32(TC_BM, a.n_sub);
+        // descriptors of stage 0; a stage, a K step (32 bytes) and an MMA's
+        // token block only move the start-address field (address >> 4)
+        const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(smem));
+        const uint32_t stage16 = (uint32_t)stage_bytes >> 4;
+        const uint32_t xsub16 = (uint32_t)(a.n_sub * TC_BK * 2) >> 4;
         const SegIter seg_it(u0, u1, a.nkb);
-        int it = 0;
+        int s = 0;
+        uint32_t ph = 0, st16 = 0;
         bool ok = true;
         for (int seg = 0; seg < seg_it.n && ok; ++seg) {
             int sa, sb;
             seg_it.get(seg, sa, sb);
             const int buf = seg % n_acc;
             const int use = seg / n_acc;
-            if (use > 0 && !mbar_wait(&acce[buf], (uint32_t)(use - 1) & 1u, abort_flag, TC_WAIT_NS)) {
-                set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                *abort_flag = 1;
+            if (use > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(&acce[buf], (uint32_t)(use - 1) & 1u, abort_flag, TC_WAIT_NS))) {
+                if (lane == 0) {
+                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                    *abort_flag = 1;
+                }
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t d0 = tmem + (uint32_t)(buf * 256);
-            for (int u = sa; u < sb; ++u, ++it) {
-                const int s = it % S;
-                if (!mbar_wait(&full[s], (uint32_t)(it / S) & 1u, abort_flag, TC_WAIT_NS)) {
-                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                    *abort_flag = 1;
+            for (int u = sa; u < sb; ++u) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, TC_WAIT_NS))) {
+                    if (lane == 0) {
+                        set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t w_base = smem_u32(smem + (size_t)s * stage_bytes);
-                const uint32_t x_base = w_base + TC_W_BYTES;
-                for (int sub = 0; sub < a.nsub; ++sub) {
+                const uint64_t dw = desc0 + st16;
+                const uint64_t dx = dw + (TC_W_BYTES >> 4);
 #pragma unroll
-                    for (int k = 0; k < TC_BK / 16; ++k)
-                        mma_bf16(d0 + (uint32_t)(sub * 256), sdesc_kmajor_sw128(w_base + k * 32),
-                                 sdesc_kmajor_sw128(x_base + sub * a.n_sub * TC_BK * 2 + k * 32), idesc,
-                                 (u > sa || k > 0) ? 1u : 0u);
+                for (int sub = 0; sub < 2; ++sub) {
+                    if (sub < a.nsub) {
+#pragma unroll
+                        for (int k = 0; k < TC_BK / 16; ++k)
+                            mma_bf16_elect(d0 + (uint32_t)(sub * 256), dw + (uint32_t)(k * 2),
+                                           dx + (uint32_t)(sub * xsub16 + k * 2), idesc,
+                                           (u > sa || k > 0) ? 1u : 0u);
+                    }
                 }
-                if (s % a.rel == a.rel - 1) {
+                if ((s & rel_mask) == rel_mask) {
                     if (a.G > 1)
-                        mma_commit_multicast(&empty[s / a.rel], mask);
+                        mma_commit_multicast_elect(&empty[s >> rel_shift], mask);
                     else
-                        mma_commit(&empty[s / a.rel]);
+                        mma_commit_elect(&empty[s >> rel_shift]);
+                }
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                    st16 = 0;
+                } else {
+                    st16 += stage16;
                 }
             }
             if (!ok)
                 break;
-            mma_commit(&accf[buf]);
+            mma_commit_elect(&accf[buf]);
         }
-        if (ok && it % S % a.rel != 0) {
+        if (ok && (s & rel_mask) != 0) {
             // release the partly used last group
-            const int s = (it - 1) % S;
             if (a.G > 1)
-                mma_commit_multicast(&empty[s / a.rel], mask);
+                mma_commit_multicast_elect(&empty[(s - 1) >> rel_shift], mask);
             else
-                mma_commit(&empty[s / a.rel]);
+                mma_commit_elect(&empty[(s - 1) >> rel_shift]);
         }
         if (!ok) {
-            mma_commit(drain);
+            mma_commit_elect(drain);
             mbar_wait(drain, 0, nullptr, TC_WAIT_NS / 4);
         }
     } else if (warp >= 2) {
         // ------------------------------------------------------ epilogue
-        // TMEM (thread = output feature, registers = tokens) is transposed
-        // through shared memory 32 tokens at a time; each thread then owns
-        // (token, 16 consecutive features) items.
+        // With the 32x32b TMEM load a lane holds one output feature (TMEM
+        // lane) and its registers hold consecutive token columns, so a warp
+        // owns 32 consecutive features of each token: plain warp-wide stores
+        // are coalesced and no shared-memory transpose is needed.  The four
+        // warps work independently on their quadrants of the 128 features.
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int et = threadIdx.x - 64;
-        const int row = q * 32 + lane;
+        const int f = q * 32 + lane;  // feature within the weight tile
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const bool partial_mode = ep.mode == EPI_PARTIAL;
         const SegIter seg_it(u0, u1, a.nkb);
@@ -315,16 +472,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int use = seg / n_acc;
             const bool whole = (kb0 == 0 && kb1 == a.nkb);
             const bool direct = whole && !partial_mode;
+            const int nb = mt * TC_BM + q * 32;  // first feature of this warp
             if (direct && ep.mode == EPI_RESID) {
-                // bring this tile's residual rows into L2 while the MMAs run
-                for (int i = et; i < a.tg * 2; i += 128) {
-                    const int t = t_base + (i >> 1);
-                    if (t < a.T)
-                        prefetch_l2(ep.resid + (size_t)t * a.N + mt * TC_BM + (i & 1) * 64);
+                // bring this warp's residual rows into L2 while the MMAs run
+                for (int c = lane; c < a.tg; c += 32) {
+                    const int t = t_base + c;
+                    if (t < a.T && nb < a.N)
+                        prefetch_l2(ep.resid + (size_t)t * a.N + nb);
                 }
             }
-            if (!mbar_wait(&accf[buf], (uint32_t)use & 1u, abort_flag, TC_WAIT_NS * 2)) {
-                if (!*abort_flag) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&accf[buf], (uint32_t)use & 1u, abort_flag, TC_WAIT_NS * 2))) {
+                if (lane == 0 && !*abort_flag) {
                     set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                     *abort_flag = 1;
                 }
@@ -334,47 +492,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
             const int slot = mt - u0 / a.nkb;
             float *ws_mine = a.ws + ((size_t)cta * a.slots + slot) * a.tg * TC_BM;
-            for (int cc = 0; cc < a.nsub * a.n_sub; cc += 32) {
-                const int sub = cc / a.n_sub, c0 = cc % a.n_sub;  // n_sub is a multiple of 32 when nsub == 2
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0 + h * 16), r);
+            for (int sub = 0; sub < a.nsub; ++sub) {
+                for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0), *reinterpret_cast<uint32_t(*)[16]>(r));
+                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0 + 16),
+                                       *reinterpret_cast<uint32_t(*)[16]>(r + 16));
                     tmem_ld_wait();
+                    const int col0 = sub * a.n_sub + c0;  // token column of r[0] in this CTA
+                    const int ncol = min(32, a.n_sub - c0);
+                    if (direct) {
+                        emit_cols(ep, s_pos, s_slot, s_xp + q * 32 * TC_XP_LD, t_base, col0, ncol, nb, lane, r);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        stg[(h * 16 + j) * TC_STG_LD + row] = __uint_as_float(r[j]);
-                }
-                epi_bar();
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int it = et + k * 128;
-                    const int j = it >> 3, gq = it & 7;
-                    const int col = sub * a.n_sub + c0 + j;
-                    if (c0 + j < a.n_sub) {
-                        const float4 *sp = reinterpret_cast<const float4 *>(stg + j * TC_STG_LD + gq * 16);
-                        float v[16];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 f = sp[e];
-                            v[4 * e] = f.x;
-                            v[4 * e + 1] = f.y;
-                            v[4 * e + 2] = f.z;
-                            v[4 * e + 3] = f.w;
-                        }
-                        if (direct) {
-                            const int t = t_base + col, n0 = mt * TC_BM + gq * 16;
-                            if (t < a.T && n0 < a.N)
-                                epi_group(ep, t, n0, v);
-                        } else {
-                            float4 *dst = reinterpret_cast<float4 *>(ws_mine + (size_t)col * TC_BM + gq * 16);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                        }
+                        for (int j = 0; j < 32; ++j)
+                            if (j < ncol)
+                                ws_mine[(size_t)(col0 + j) * TC_BM + f] = __uint_as_float(r[j]);
                     }
                 }
-                epi_bar();
             }
             // accumulator buffer free for the MMA warp
             tc_fence_before();
@@ -394,31 +529,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 epi_bar();
                 if (*last_flag) {
                     __threadfence();
-                    for (int it = et; it < a.tg * 8; it += 128) {
-                        const int col = it >> 3, gq = it & 7;
-                        const int t = t_base + col, n0 = mt * TC_BM + gq * 16;
-                        if (t >= a.T || n0 >= a.N)
-                            continue;
-                        float v[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            v[e] = 0.f;
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const int cslot = mt - unit_begin(c, a) / a.nkb;
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                a.ws + (((size_t)(c * a.G + rank) * a.slots + cslot) * a.tg + col) * TC_BM +
-                                gq * 16);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float4 f = __ldcg(src + e);
-                                v[4 * e] += f.x;
-                                v[4 * e + 1] += f.y;
-                                v[4 * e + 2] += f.z;
-                                v[4 * e + 3] += f.w;
-                            }
-                        }
-                        epi_group(ep, t, n0, v);
-                    }
+                    fixup_tile(ep, a, s_pos, s_slot, s_xp + q * 32 * TC_XP_LD, rank, t_base, mt, c_lo, c_hi, nb, f,
+                               lane);
                     if (et == 0)
                         a.counters[tile] = 0;
                 }
@@ -586,6 +698,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf
     a.nsub = sh.nsub;
     a.n_sub = sh.n_sub;
     a.tg = sh.tg;
+    a.n_sub32 = (sh.n_sub + 31) / 32 * 32;
     {
         int piece = (TC_BM + a.G - 1) / a.G;
         piece = (piece + 7) / 8 * 8;  // whole 1 KB swizzle atoms
@@ -648,7 +761,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf
     a.ws = rt.ws;
     a.counters = rt.counters;
     a.w_tiled = W_tiled;
-    a.rel = (a.tg < 224) ? 2 : 1;
+    a.rel = (a.tg < 224) ? 2 : 1;  // 1 or 2: the kernel's ring counters assume a power of two <= 2
     CUtensorMap tmX;
     if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.n_sub))
         return cudaErrorInvalidValue;

@@ -130,6 +130,66 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// ------------------------------------------------- warp-wide issue helpers
+// The producer and MMA roles run their loops on a whole converged warp, so
+// every address, coordinate and descriptor is warp-uniform and the compiler
+// keeps it in uniform registers; one lane, chosen by elect.sync inside the
+// same asm statement, issues the asynchronous operation.  Issuing from a
+// single-lane branch instead costs a uniform-register conversion per
+// operation, which made the issuing thread (not memory, not the tensor
+// pipe) the bottleneck of the small-N GEMM.  Every lane of the warp must
+// execute these together.
+
+__device__ __forceinline__ void mbar_expect_tx_elect(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+        "}\n" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_elect(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];\n"
+        "}\n" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_multicast_elect(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
+                                                            int c1, uint16_t cta_mask)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;\n"
+        "}\n" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2_elect(const void *src, uint32_t bytes)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.prefetch.L2.global [%0], %1;\n"
+        "}\n" ::"l"((uint64_t)src),
+        "r"(bytes)
+        : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
@@ -176,6 +236,45 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
+// Warp-wide forms of mma_bf16 / mma_commit / mma_commit_multicast (see the
+// issue helpers above).
+__device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p, e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint64_t *bar)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+        "}\n" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_multicast_elect(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
+        "}\n" ::"r"(smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
 }
