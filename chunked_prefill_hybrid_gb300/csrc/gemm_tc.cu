@@ -60,6 +60,7 @@ struct TcArgs {
     int n_sub;        // tokens per MMA (multiple of 16, <= 256); a CTA holds tg = nsub * n_sub
     int tg;
     int n_sub32;      // n_sub rounded up to 32 (the epilogue's column chunks)
+    int nslot;        // pair kernel: TMEM accumulator slots of n_sub columns
     int wpiece;       // weight-tile rows each CTA fetches and multicasts
     int units, grid;  // units = n_mtiles * nkb over `grid` clusters
     int stages, slots;
@@ -548,6 +549,316 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 }
 
+// ------------------------------------------------------------ pair kernel
+// The same linear op on CTA pairs (clusters of two) with the 2-SM MMA: one
+// tcgen05.mma.cta_group::2 computes a 256-row x n_sub-token product whose
+// rows are two weight tiles, one in each CTA, and whose tokens are split
+// between the pair's shared memories (the even CTA holds the first n_sub/2
+// of each MMA's tokens, the odd CTA the rest).  Per SM that halves both the
+// MMA instructions and the shared-memory fill for a given amount of work
+// compared with one CTA per tile, so the weight stream (the HBM bound of
+// these small-T products) rather than the issue loop sets the pace.
+//
+// Work: stream-K over units (weight-tile pair, k-block); a pair's unit range
+// is cut into segments at tile-pair boundaries.  CTA r of a pair owns weight
+// tile 2p + r of tile pair p for all T tokens (nsub MMAs of n_sub tokens).
+// TMEM is a ring of nslot slots of n_sub columns; a segment takes nsub
+// consecutive slots, and the epilogue releases each slot as soon as it has
+// read it, so the next segment starts before the previous one is drained.
+//   warp 0      TMA producer in both CTAs: own weight tile + own token
+//               halves, completing on the leader's full barrier
+//   warp 1      TMEM allocation (both CTAs); MMA issue (even CTA only)
+//   warps 2..5  epilogue in both CTAs on their own TMEM rows
+constexpr int TC_MAX_SLOTS = 4;
+constexpr int TC_PAIR_CTRL = 512;
+
+__host__ __device__ inline int pair_stage_bytes(int nsub, int n_sub) { return TC_W_BYTES + nsub * (n_sub / 2) * TC_BK * 2; }
+__host__ __device__ inline int pair_smem_bytes(int nsub, int n_sub, int stages)
+{
+    return stages * pair_stage_bytes(nsub, n_sub) + TC_PAIR_CTRL + TC_META_BYTES + TC_XP_BYTES + 1024;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
+                EpiParams ep)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int S = a.stages;
+    const int xhalf = a.n_sub >> 1;  // token rows of one MMA held by this CTA
+    const int stage_bytes = pair_stage_bytes(a.nsub, a.n_sub);
+    uint64_t *full = (uint64_t *)(smem + (size_t)S * stage_bytes);  // [S] (the leader's count)
+    uint64_t *empty = full + S;                                     // [S / rel]
+    uint64_t *accf = empty + S;                                     // [4]
+    uint64_t *sfree = accf + 4;                                     // [TC_MAX_SLOTS] (leader)
+    uint64_t *drain = sfree + TC_MAX_SLOTS;
+    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
+    int *s_pos = (int *)(smem + (size_t)S * stage_bytes + TC_PAIR_CTRL);
+    int *s_slot = s_pos + TC_MAX_TG;
+    float *s_xp = (float *)(s_slot + TC_MAX_TG);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = (int)cluster_ctarank();  // 0: the pair's leader
+    const int clu = blockIdx.x >> 1;
+    const int cta = clu * 2 + r;
+    const int u0 = unit_begin(clu, a), u1 = unit_begin(clu + 1, a);
+    const int rel_mask = a.rel - 1, rel_shift = a.rel == 2 ? 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i)
+            mbar_init(&full[i], 1);
+        for (int i = 0; i < S / a.rel; ++i)
+            mbar_init(&empty[i], 1);  // the leader's commit, multicast to both CTAs
+        for (int i = 0; i < 4; ++i)
+            mbar_init(&accf[i], 1);
+        for (int i = 0; i < TC_MAX_SLOTS; ++i)
+            mbar_init(&sfree[i], 8);  // every epilogue warp of both CTAs
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (ep.mode == EPI_QKV)
+        for (int c = threadIdx.x; c < a.tg; c += TC_THREADS) {
+            s_pos[c] = c < a.T ? ep.pos[c] : 0;
+            s_slot[c] = c < a.T ? ep.slot[c] : -1;
+        }
+    if (warp == 1)
+        tmem_alloc_pair(tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any copy or MMA
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t full_leader = cluster_map(smem_u32(full), 0);
+    const uint32_t sfree_leader = cluster_map(smem_u32(sfree), 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        const uint32_t bytes = (uint32_t)(2 * stage_bytes);  // both CTAs' copies land on the leader's barrier
+        const SegIter seg_it(u0, u1, a.nkb);
+        int it = 0, s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int i = 0; i < seg_it.n && ok; ++i) {
+            int sa, sb;
+            seg_it.get(i, sa, sb);
+            const int mp = sa / a.nkb;
+            const int tile = 2 * mp + r;
+            const bool real = tile < a.n_mtiles;  // an odd tile count pads the last pair
+            int kb = sa - mp * a.nkb;
+            const bf16 *wbase = a.w_tiled + (size_t)tile * a.nkb * TC_BM * TC_BK;
+            if (real)
+                for (int k = kb; k < min(kb + (sb - sa), kb + TC_PREFETCH); ++k)
+                    bulk_prefetch_l2_elect(wbase + (size_t)k * TC_BM * TC_BK, TC_W_BYTES);
+            for (int u = sa; u < sb; ++u, ++it, ++kb) {
+                if (real && u + TC_PREFETCH < sb)
+                    bulk_prefetch_l2_elect(wbase + (size_t)(kb + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES);
+                if (it >= S && (s & rel_mask) == 0 &&
+                    !__all_sync(0xffffffffu, mbar_wait(&empty[s >> rel_shift], ph ^ 1u, abort_flag, TC_WAIT_NS))) {
+                    if (lane == 0) {
+                        set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+                uint8_t *sw = smem + (size_t)s * stage_bytes;
+                const uint32_t fb = full_leader + (uint32_t)(s * 8);
+                if (r == 0)
+                    mbar_expect_tx_elect(&full[s], bytes);
+                tma_load_2d_pair_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM);
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub)
+                    if (sub < a.nsub)
+                        tma_load_2d_pair_elect(sw + TC_W_BYTES + sub * xhalf * TC_BK * 2, &tmX, fb, kb * TC_BK,
+                                               sub * a.n_sub + r * xhalf);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        // tail: every stage this CTA filled has been consumed (the leader's
+        // commits), so no copy into this CTA is still in flight
+        for (int k = (it > S ? it - S : 0); k < it; ++k)
+            if (k % S % a.rel == 0)
+                mbar_wait(&empty[(k % S) / a.rel], (uint32_t)(k / S) & 1u, ok ? abort_flag : nullptr,
+                          ok ? TC_WAIT_NS : TC_WAIT_NS / 4);
+    } else if (warp == 1) {
+        if (r == 0) {
+            // -------------------------------------------------- MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(2 * TC_BM, a.n_sub);
+            const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(smem));
+            const uint32_t stage16 = (uint32_t)stage_bytes >> 4;
+            const uint32_t xsub16 = (uint32_t)(xhalf * TC_BK * 2) >> 4;
+            const SegIter seg_it(u0, u1, a.nkb);
+            int s = 0, slot_next = 0;
+            uint32_t ph = 0, st16 = 0, seen = 0, par = 0;
+            bool ok = true;
+            for (int seg = 0; seg < seg_it.n && ok; ++seg) {
+                int sa, sb;
+                seg_it.get(seg, sa, sb);
+                uint32_t dcol[2];
+#pragma unroll
+                for (int sub = 0; sub < 2; ++sub) {
+                    if (sub < a.nsub) {
+                        const int j = slot_next;
+                        slot_next = slot_next + 1 == a.nslot ? 0 : slot_next + 1;
+                        dcol[sub] = (uint32_t)(j * a.n_sub);
+                        if ((seen >> j) & 1u) {
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(&sfree[j], (par >> j) & 1u, abort_flag, TC_WAIT_NS))) {
+                                if (lane == 0) {
+                                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                                    *abort_flag = 1;
+                                }
+                                ok = false;
+                            }
+                            par ^= 1u << j;
+                        }
+                        seen |= 1u << j;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc_fence_after();
+                for (int u = sa; u < sb; ++u) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, TC_WAIT_NS))) {
+                        if (lane == 0) {
+                            set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t dw = desc0 + st16;
+                    const uint64_t dx = dw + (TC_W_BYTES >> 4);
+#pragma unroll
+                    for (int sub = 0; sub < 2; ++sub) {
+                        if (sub < a.nsub) {
+#pragma unroll
+                            for (int k = 0; k < TC_BK / 16; ++k)
+                                mma_bf16_pair_elect(tmem + dcol[sub], dw + (uint32_t)(k * 2),
+                                                    dx + (uint32_t)(sub * xsub16 + k * 2), idesc,
+                                                    (u > sa || k > 0) ? 1u : 0u);
+                        }
+                    }
+                    if ((s & rel_mask) == rel_mask)
+                        mma_commit_pair_elect(&empty[s >> rel_shift]);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                        st16 = 0;
+                    } else {
+                        st16 += stage16;
+                    }
+                }
+                if (!ok)
+                    break;
+                mma_commit_pair_elect(&accf[seg & 3]);
+            }
+            if (ok && (s & rel_mask) != 0)
+                mma_commit_pair_elect(&empty[(s - 1) >> rel_shift]);
+            if (!ok) {
+                mma_commit_pair_elect(drain);
+                mbar_wait(drain, 0, nullptr, TC_WAIT_NS / 4);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int et = threadIdx.x - 64;
+        const int f = q * 32 + lane;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const bool partial_mode = ep.mode == EPI_PARTIAL;
+        float *xp = s_xp + q * 32 * TC_XP_LD;
+        const SegIter seg_it(u0, u1, a.nkb);
+        int slot_next = 0;
+        for (int seg = 0; seg < seg_it.n; ++seg) {
+            int sa, sb;
+            seg_it.get(seg, sa, sb);
+            const int mp = sa / a.nkb, kb0 = sa % a.nkb;
+            const int kb1 = kb0 + (sb - sa);
+            const int tile = 2 * mp + r;
+            const bool whole = (kb0 == 0 && kb1 == a.nkb);
+            const bool direct = whole && !partial_mode;
+            const int nb = tile * TC_BM + q * 32;
+            if (direct && ep.mode == EPI_RESID) {
+                for (int c = lane; c < a.tg; c += 32)
+                    if (c < a.T && nb < a.N)
+                        prefetch_l2(ep.resid + (size_t)c * a.N + nb);
+            }
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&accf[seg & 3], (uint32_t)(seg >> 2) & 1u, abort_flag, TC_WAIT_NS * 2))) {
+                if (lane == 0 && !*abort_flag) {
+                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const int wslot = mp - u0 / a.nkb;
+            float *ws_mine = a.ws + ((size_t)cta * a.slots + wslot) * a.tg * TC_BM;
+            for (int sub = 0; sub < a.nsub; ++sub) {
+                const int j = slot_next;
+                slot_next = slot_next + 1 == a.nslot ? 0 : slot_next + 1;
+                const uint32_t d0 = tmem + lane_base + (uint32_t)(j * a.n_sub);
+                for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
+                    uint32_t rr[32];
+                    tmem_ld_32x32b_x16(d0 + (uint32_t)c0, *reinterpret_cast<uint32_t(*)[16]>(rr));
+                    tmem_ld_32x32b_x16(d0 + (uint32_t)(c0 + 16), *reinterpret_cast<uint32_t(*)[16]>(rr + 16));
+                    tmem_ld_wait();
+                    const int col0 = sub * a.n_sub + c0;
+                    const int ncol = min(32, a.n_sub - c0);
+                    if (direct) {
+                        emit_cols(ep, s_pos, s_slot, xp, 0, col0, ncol, nb, lane, rr);
+                    } else {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            if (jj < ncol)
+                                ws_mine[(size_t)(col0 + jj) * TC_BM + f] = __uint_as_float(rr[jj]);
+                    }
+                }
+                // this slot's columns are read: hand them back to the MMA warp
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_remote_arrive(sfree_leader + (uint32_t)(j * 8));
+            }
+            if (!whole && !partial_mode) {
+                __threadfence();
+                epi_bar();
+                const int c_lo = unit_owner((long long)mp * a.nkb, a);
+                const int c_hi = unit_owner((long long)mp * a.nkb + a.nkb - 1, a);
+                if (et == 0) {
+                    const int old = atomicAdd(&a.counters[tile], 1);
+                    *last_flag = (old == c_hi - c_lo);
+                }
+                epi_bar();
+                if (*last_flag) {
+                    __threadfence();
+                    fixup_tile(ep, a, s_pos, s_slot, xp, r, 0, mp, c_lo, c_hi, nb, f, lane);
+                    if (et == 0)
+                        a.counters[tile] = 0;
+                }
+                epi_bar();
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs and both epilogues are done with both CTAs
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
 // Rearrange W [N][K] (rows optionally permuted) into [n_tile][k_block][128][64],
 // zero outside N x K.  mode 0: identity rows; 1: RoPE pair permutation
 // within heads of `a` rows; 2: gate/up interleave with ffn = `a`.
@@ -757,6 +1068,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf
         part->nkb = a.nkb;
         part->tg = a.tg;
         part->slots = a.slots;
+        part->pair = 0;
     }
     a.ws = rt.ws;
     a.counters = rt.counters;
@@ -767,6 +1079,139 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf
         return cudaErrorInvalidValue;
     cfg.gridDim = dim3((unsigned)(a.grid * a.G));
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, tmW, tmX, a, ep);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------- pair launcher
+TcShape tc_pair_shape(int T)
+{
+    TcShape sh;
+    sh.G = 2;
+    sh.nsub = T <= 256 ? 1 : 2;
+    sh.n_sub = ((T + sh.nsub - 1) / sh.nsub + 15) / 16 * 16;
+    if (sh.n_sub < 16)
+        sh.n_sub = 16;
+    sh.tg = sh.nsub * sh.n_sub;
+    return sh;
+}
+
+static int pair_nslot(int n_sub)
+{
+    int n = 512 / n_sub;
+    if (n > TC_MAX_SLOTS)
+        n = TC_MAX_SLOTS;
+    while (n > 0 && (n - 1) * n_sub + (n_sub + 31) / 32 * 32 > 512)
+        --n;  // the epilogue reads whole 32-column chunks
+    return n;
+}
+
+size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes)
+{
+    size_t need = 0;
+    for (int i = 0; i < n_shapes; ++i)
+        for (int T = 1; T <= max_tokens && T <= TC_PAIR_MAX_T; ++T) {
+            const TcShape sh = tc_pair_shape(T);
+            const int n_mpairs = ((Ns[i] + TC_BM - 1) / TC_BM + 1) / 2;
+            const int nkb = (Ks[i] + TC_BK - 1) / TC_BK;
+            const long long units = (long long)n_mpairs * nkb;
+            const int grid = tc_grid(units, num_sms / 2);
+            const size_t n = (size_t)grid * 2 * tc_slots(units, grid, nkb) * sh.tg * TC_BM;
+            if (n > need)
+                need = n;
+        }
+    return need;
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
+                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part)
+{
+    if (T <= 0)
+        return cudaSuccess;
+    if (K % 8 != 0 || T > TC_PAIR_MAX_T)
+        return cudaErrorInvalidValue;
+    const TcShape sh = tc_pair_shape(T);
+    TcArgs a = {};
+    a.T = T;
+    a.N = N;
+    a.K = K;
+    a.n_mtiles = (N + TC_BM - 1) / TC_BM;
+    a.nkb = (K + TC_BK - 1) / TC_BK;
+    a.G = 2;
+    a.nsub = sh.nsub;
+    a.n_sub = sh.n_sub;
+    a.tg = sh.tg;
+    a.n_sub32 = (sh.n_sub + 31) / 32 * 32;
+    a.nslot = pair_nslot(sh.n_sub);
+    if (a.nslot < a.nsub || a.tg > TC_MAX_TG)
+        return cudaErrorInvalidValue;
+    a.wpiece = TC_BM;
+    const int n_mpairs = (a.n_mtiles + 1) / 2;
+    const long long units = (long long)n_mpairs * a.nkb;
+    if (units > (1ll << 30) || (long long)n_mpairs * 2 > rt.n_counters)
+        return cudaErrorInvalidValue;
+    a.units = (int)units;
+    a.rel = (a.tg < 224) ? 2 : 1;  // 1 or 2: the kernel's ring counters assume a power of two <= 2
+    int stages = 12;
+    while (stages > 2 && pair_smem_bytes(a.nsub, a.n_sub, stages) > rt.max_smem)
+        stages -= a.rel;
+    if (pair_smem_bytes(a.nsub, a.n_sub, stages) > rt.max_smem || stages % a.rel)
+        return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    const int smem = pair_smem_bytes(a.nsub, a.n_sub, stages);
+    static int configured = 0;
+    if (configured < rt.max_smem) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, rt.max_smem);
+        if (e != cudaSuccess)
+            return e;
+        configured = rt.max_smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static int max_pairs[13] = {};
+    int &mc = max_pairs[stages];
+    if (!mc) {
+        cfg.gridDim = dim3((unsigned)(rt.num_sms / 2 * 2));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = rt.num_sms / 2;
+        }
+        mc = n < rt.num_sms / 2 ? n : rt.num_sms / 2;
+    }
+    a.grid = tc_grid(units, mc);
+    a.slots = tc_slots(units, a.grid, a.nkb);
+    if ((size_t)a.grid * 2 * a.slots * a.tg * TC_BM > rt.ws_floats)
+        return cudaErrorInvalidValue;
+    if (part) {
+        part->ws = rt.ws;
+        part->grid = a.grid;
+        part->G = 2;
+        part->units = a.units;
+        part->nkb = a.nkb;
+        part->tg = a.tg;
+        part->slots = a.slots;
+        part->pair = 1;
+    }
+    a.ws = rt.ws;
+    a.counters = rt.counters;
+    a.w_tiled = W_tiled;
+    CUtensorMap tmX;
+    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)(a.n_sub / 2)))
+        return cudaErrorInvalidValue;
+    cfg.gridDim = dim3((unsigned)(a.grid * 2));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair, tmW, tmX, a, ep);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();

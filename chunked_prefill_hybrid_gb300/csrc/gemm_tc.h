@@ -29,10 +29,30 @@ struct TcRuntime {
 // r*tg ..).  Cluster c's rank-r CTA keeps its share of tile mt at slot
 // (mt - first tile of c), element [col][feature % 128] of
 // ws + (((c * G + r) * slots + slot) * tg) * 128.
+// Pair kernel (pair = 1): units are (weight-tile pair, k-block) over `grid`
+// CTA pairs; CTA r of pair c holds weight tile 2p + r for all T tokens
+// (col = token) at slot (p - first tile pair of c) of
+// ws + (((c * 2 + r) * slots + slot) * tg) * 128.
 struct TcPartition {
     const float *ws = nullptr;
     int grid = 0, G = 1, units = 0, nkb = 0, tg = 0, slots = 0;
+    int pair = 0;
 };
+
+// Unit row (tile or tile pair), CTA rank and token column holding the
+// partials of output (t, feature tile mt) in a partition.
+__host__ __device__ inline void tc_part_loc(const TcPartition &p, int t, int mt, int &urow, int &r, int &col)
+{
+    if (p.pair) {
+        urow = mt >> 1;
+        r = mt & 1;
+        col = t;
+    } else {
+        urow = mt;
+        r = t / p.tg;
+        col = t % p.tg;
+    }
+}
 
 // Workspace floats needed for any batch of up to max_tokens rows and the
 // given (N, K) shapes.
@@ -47,6 +67,16 @@ cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mo
 bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, int box_rows);
 int tc_weight_box_rows(int T);
 
+// Largest batch one pair-kernel launch takes (callers cut larger ones).
+constexpr int TC_PAIR_MAX_T = 512;
+TcShape tc_pair_shape(int T);
+size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes);
+
+// The same product on CTA pairs with the 2-SM MMA (T <= TC_PAIR_MAX_T);
+// tmW must use 128-row boxes.
+cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
+                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr);
+
 // acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
 // tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).
 // W_tiled: the tiled weights tmW describes (streamed into L2 ahead of use).
@@ -59,7 +89,8 @@ cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16
                                const float *gamma, bf16 *norm_out, float eps, cudaStream_t s);
 
 // Finish a partial-mode GEMM: sum each (token, 16 stored features) group's
-// partials in cluster order and apply ep's fused epilogue (ep.N % 16 == 0).
+// partials in contributor order and apply ep's fused epilogue (ep.N % 16 == 0
+// except for EPI_F32).
 cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s);
 
 }  // namespace hb

@@ -67,6 +67,9 @@ int hb_init_fast_path(hb_ctx *ctx)
         const int Ns[4] = {ctx->n_qkv, c.hidden, ctx->n_gu, c.hidden};
         const int Ks[4] = {c.hidden, c.n_heads * c.head_dim, c.hidden, c.ffn};
         rt.ws_floats = tc_workspace_floats(ctx->num_sms, c.max_tokens, Ns, Ks, 4);
+        const size_t pair_floats = tc_pair_workspace_floats(ctx->num_sms, c.max_tokens, Ns, Ks, 4);
+        if (rt.ws_floats < pair_floats)
+            rt.ws_floats = pair_floats;
         const size_t floor_floats = (size_t)ctx->num_sms * 2 * 512 * 128;  // room for hb_gemm_test shapes
         if (rt.ws_floats < floor_floats)
             rt.ws_floats = floor_floats;
@@ -106,7 +109,7 @@ int hb_init_fast_path(hb_ctx *ctx)
                 return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
         }
     }
-    ctx->gemm_impl = 1;
+    ctx->gemm_impl = 2;
     ctx->attn_impl = 1;
     return HB_OK;
 }
@@ -155,7 +158,18 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
     } while (0)
 
 // Largest token slab of one tensor-core GEMM launch (8 token groups of 256).
-constexpr int kSlab = 2048;
+constexpr int kSlab = 2048;  // rows per launch of the token-group kernel
+// rows per launch of the selected tensor-core kernel
+static int slab_rows(const hb_ctx *ctx) { return ctx->gemm_impl == 2 ? TC_PAIR_MAX_T : kSlab; }
+
+// One launch of the selected tensor-core kernel (token groups or CTA pairs).
+static cudaError_t launch_tc(const hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *W, const bf16 *X, int T,
+                             int N, int K, const EpiParams &ep, TcPartition *part = nullptr)
+{
+    if (ctx->gemm_impl == 2)
+        return launch_gemm_pair(M.m[kind][0], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part);
+    return launch_gemm_tc(M.get(kind, T), W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part);
+}
 
 // The epilogue parameters of rows [t0, t0 + Tn) of a batch.
 static EpiParams epi_rows(const EpiParams &ep, int t0, int Tn)
@@ -186,11 +200,29 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
 {
     if (ctx->gemm_impl == 0)
         return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
-    ctx->n_launches += (T + kSlab - 1) / kSlab - 1;  // one is counted by the caller
-    for (int t0 = 0; t0 < T; t0 += kSlab) {
-        const int Tn = T - t0 < kSlab ? T - t0 : kSlab;
-        cudaError_t e = launch_gemm_tc(M.get(kind, Tn), W, X + (size_t)t0 * K, Tn, N, K, epi_rows(ep, t0, Tn),
-                                       ctx->fast->rt, ctx->stream);
+    const int slab = slab_rows(ctx);
+    const bool pair = ctx->gemm_impl == 2;
+    // the pair kernel leaves fp32 partial tiles; a grid-wide pass sums them
+    // and applies the fused epilogue
+    ctx->n_launches += (pair ? 2 : 1) * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
+    for (int t0 = 0; t0 < T; t0 += slab) {
+        const int Tn = T - t0 < slab ? T - t0 : slab;
+        const EpiParams er = epi_rows(ep, t0, Tn);
+        if (!pair) {
+            cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, er);
+            if (e != cudaSuccess)
+                return e;
+            continue;
+        }
+        EpiParams pp{};
+        pp.mode = EPI_PARTIAL;
+        pp.T = Tn;
+        pp.N = N;
+        pp.err = ep.err;
+        TcPartition part;
+        cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, pp, &part);
+        if (e == cudaSuccess)
+            e = launch_reduce_epi(part, er, ctx->stream);
         if (e != cudaSuccess)
             return e;
     }
@@ -203,15 +235,15 @@ static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const 
                                int K, const bf16 *resid, bf16 *out, const float *gamma, bf16 *norm_out, int *launches)
 {
     const hb_model_config &c = ctx->cfg;
-    for (int t0 = 0; t0 < T; t0 += kSlab) {
-        const int Tn = T - t0 < kSlab ? T - t0 : kSlab;
+    const int slab = slab_rows(ctx);
+    for (int t0 = 0; t0 < T; t0 += slab) {
+        const int Tn = T - t0 < slab ? T - t0 : slab;
         EpiParams pp{};
         pp.mode = EPI_PARTIAL;
         pp.T = Tn;
         pp.N = N;
         TcPartition part;
-        cudaError_t e = launch_gemm_tc(M.get(kind, Tn), W, X + (size_t)t0 * K, Tn, N, K, pp, ctx->fast->rt,
-                                       ctx->stream, &part);
+        cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, pp, &part);
         if (e != cudaSuccess)
             return e;
         e = launch_reduce_norm(part, Tn, N, resid + (size_t)t0 * N, out + (size_t)t0 * N, gamma,
@@ -355,12 +387,27 @@ extern "C" int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, 
         f->test_w_elems = need;
     }
     CUtensorMap tm;
-    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K, tc_weight_box_rows(T)))
+    const bool pair = ctx->gemm_impl == 2;
+    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K, pair ? 128 : tc_weight_box_rows(T)))
         return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed");
     ctx->n_launches++;
     if (launch_tile_weights((const bf16 *)W, f->test_w, N, K, 0, 0, ctx->stream) != cudaSuccess)
         return ctx->set_error(HB_ECUDA, "tile launch failed");
-    LK(K_GEMM_TEST, launch_gemm_tc(tm, f->test_w, (const bf16 *)X, T, N, K, ep, f->rt, ctx->stream));
+    if (!pair) {
+        LK(K_GEMM_TEST, launch_gemm_tc(tm, f->test_w, (const bf16 *)X, T, N, K, ep, f->rt, ctx->stream));
+        return HB_OK;
+    }
+    for (int t0 = 0; t0 < T; t0 += TC_PAIR_MAX_T) {
+        const int Tn = T - t0 < TC_PAIR_MAX_T ? T - t0 : TC_PAIR_MAX_T;
+        EpiParams pp{};
+        pp.mode = EPI_PARTIAL;
+        pp.T = Tn;
+        pp.N = N;
+        TcPartition part;
+        LK(K_GEMM_TEST, launch_gemm_pair(tm, f->test_w, (const bf16 *)X + (size_t)t0 * K, Tn, N, K, pp, f->rt,
+                                         ctx->stream, &part));
+        LK(K_GEMM_TEST, launch_reduce_epi(part, epi_rows(ep, t0, Tn), ctx->stream));
+    }
     return HB_OK;
 }
 
@@ -368,8 +415,8 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
 {
     if (!ctx)
         return HB_EINVAL;
-    if (gemm_impl < 0 || gemm_impl > 1 || attn_impl < 0 || attn_impl > 1)
-        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl and attn_impl must be 0 or 1");
+    if (gemm_impl < 0 || gemm_impl > 2 || attn_impl < 0 || attn_impl > 1)
+        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0, 1 or 2 and attn_impl 0 or 1");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
     return HB_OK;

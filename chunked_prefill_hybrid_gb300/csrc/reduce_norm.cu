@@ -35,7 +35,6 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
 {
     const int t = blockIdx.x;
     const TcPartition &p = a.part;
-    const int r = t / p.tg, col = t % p.tg;
     float h[RN_MAX_GROUPS][8];
     float ss = 0.f;
 #pragma unroll
@@ -43,7 +42,8 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
         const int n0 = (threadIdx.x + i * RN_THREADS) * 8;
         if (n0 >= a.N)
             break;
-        const int mt = n0 >> 7;
+        int mt, r, col;
+        tc_part_loc(p, t, n0 >> 7, mt, r, col);
         const long long u0 = (long long)mt * p.nkb;
         const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
         float acc[8];
@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
             acc[6] += x1.z;
             acc[7] += x1.w;
         }
-        const uint4 r = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
-        const bf16 *re = reinterpret_cast<const bf16 *>(&r);
+        const uint4 rv = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
+        const bf16 *re = reinterpret_cast<const bf16 *>(&rv);
         float o[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -108,12 +108,12 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
 __global__ void __launch_bounds__(128) k_reduce_epi(TcPartition p, EpiParams ep)
 {
     const int t = blockIdx.x;
-    const int r = t / p.tg, col = t % p.tg;
     {
         const int n0 = (blockIdx.y * 128 + threadIdx.x) * 16;
         if (n0 >= ep.N)
             return;
-        const int mt = n0 >> 7;
+        int mt, r, col;
+        tc_part_loc(p, t, n0 >> 7, mt, r, col);
         const long long u0 = (long long)mt * p.nkb;
         const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
         float v[16];
@@ -143,9 +143,9 @@ cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cuda
 {
     if (ep.T <= 0)
         return cudaSuccess;
-    if (ep.N % 16 != 0)
+    if (ep.N % 16 != 0 && ep.mode != EPI_F32)  // fp32 output has a scalar tail
         return cudaErrorInvalidValue;
-    dim3 grid(ep.T, (ep.N / 16 + 127) / 128);
+    dim3 grid(ep.T, ((ep.N + 15) / 16 + 127) / 128);
     k_reduce_epi<<<grid, 128, 0, s>>>(part, ep);
     return cudaGetLastError();
 }

@@ -279,6 +279,83 @@ __device__ __forceinline__ void mma_commit_multicast_elect(uint64_t *bar, uint16
         : "memory");
 }
 
+// ------------------------------------------------------ CTA pairs (2-SM MMA)
+// With .cta_group::2 one MMA spans the two CTAs of a cluster pair: each CTA
+// holds its own 128 rows of A and half of B's N columns (the even CTA the
+// first N/2, the odd CTA the rest, each at the same shared-memory offset),
+// and each CTA's TMEM receives its 128 rows x N accumulator.  The even CTA
+// issues the MMAs and commits; TMEM is allocated by one warp in each CTA.
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// TMA 2D load into this CTA's shared memory whose completion is counted on
+// an mbarrier given by cluster address (the pair leader's barrier).
+__device__ __forceinline__ void tma_load_2d_pair_elect(void *dst, const CUtensorMap *m, uint32_t bar_cluster, int c0,
+                                                       int c1)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n"
+        "}\n" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)m), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p, e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at this offset in both CTAs of the pair once every
+// pair MMA issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit_pair_elect(uint64_t *bar)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
+        "}\n" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
 // 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp gets
 // TMEM lane (warp's quadrant base + i), columns col..col+15.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])

@@ -181,8 +181,9 @@ long long hb_launch_count(hb_ctx *ctx);
 int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int N, int K);
 
 /* Test hook: choose the kernels later calls use.  gemm_impl 0 = reference
- * SIMT GEMM, 1 = tcgen05 tensor-core GEMM (default); attn_impl 0 = one CTA
- * per (row, head), 1 = the paged hybrid-attention kernel (default).  Every
+ * SIMT GEMM, 1 = tcgen05 GEMM on clusters of token groups, 2 = tcgen05 GEMM
+ * on CTA pairs with the 2-SM MMA (default); attn_impl 0 = one CTA per
+ * (row, head), 1 = the paged hybrid-attention kernel (default).  Every
  * setting computes the same function. */
 int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl);
 

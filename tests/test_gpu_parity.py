@@ -74,7 +74,7 @@ def check_kv(ctx, w, pools, layer=0):
 # head_dim 128 and grouped-query shapes at a size the oracle finishes quickly
 D128 = synth.ModelDims(hidden=256, n_heads=2, n_kv_heads=2, head_dim=128, ffn=512)
 GQA = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn=384)
-KERNELS = {"tc+hybrid": (1, 1), "tc+simple": (1, 0), "simt+hybrid": (0, 1)}
+KERNELS = {"pair+hybrid": (2, 1), "tc+hybrid": (1, 1), "tc+simple": (1, 0), "simt+hybrid": (0, 1)}
 
 
 def _tiny(seed, chunk_offset, chunk_len, ctxs, n_layers=1, gamma="ones", dims=synth.TINY):
@@ -185,7 +185,7 @@ def test_piggybacked_decode_matches_alone():
         assert ok, (j, st)
 
 
-@pytest.mark.parametrize("impl", [0, 1], ids=["simt", "tcgen05"])
+@pytest.mark.parametrize("impl", [0, 1, 2], ids=["simt", "tcgen05", "pair"])
 @pytest.mark.parametrize("T,N,K", [(1, 256, 256), (18, 768, 256), (68, 1376, 688), (274, 512, 5120),
                                    (300, 384, 1024), (513, 256, 512), (16, 130, 64), (1100, 640, 192),
                                    (1500, 384, 128), (2048, 256, 64)])
