@@ -639,6 +639,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------ producer
         const uint32_t bytes = (uint32_t)(2 * stage_bytes);  // both CTAs' copies land on the leader's barrier
+        const uint64_t wpol = l2_policy_evict_first();
         const SegIter seg_it(u0, u1, a.nkb);
         int it = 0, s = 0;
         uint32_t ph = 0;
@@ -653,10 +654,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const bf16 *wbase = a.w_tiled + (size_t)tile * a.nkb * TC_BM * TC_BK;
             if (real)
                 for (int k = kb; k < min(kb + (sb - sa), kb + TC_PREFETCH); ++k)
-                    bulk_prefetch_l2_elect(wbase + (size_t)k * TC_BM * TC_BK, TC_W_BYTES);
+                    bulk_prefetch_l2_hint_elect(wbase + (size_t)k * TC_BM * TC_BK, TC_W_BYTES, wpol);
             for (int u = sa; u < sb; ++u, ++it, ++kb) {
                 if (real && u + TC_PREFETCH < sb)
-                    bulk_prefetch_l2_elect(wbase + (size_t)(kb + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES);
+                    bulk_prefetch_l2_hint_elect(wbase + (size_t)(kb + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES, wpol);
                 if (it >= S && (s & rel_mask) == 0 &&
                     !__all_sync(0xffffffffu, mbar_wait(&empty[s >> rel_shift], ph ^ 1u, abort_flag, TC_WAIT_NS))) {
                     if (lane == 0) {
@@ -670,7 +671,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t fb = full_leader + (uint32_t)(s * 8);
                 if (r == 0)
                     mbar_expect_tx_elect(&full[s], bytes);
-                tma_load_2d_pair_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM);
+                tma_load_2d_pair_hint_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM, wpol);
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub)
                     if (sub < a.nsub)

@@ -31,10 +31,84 @@ __device__ __forceinline__ int owner(long long u, const TcPartition &p)
 }
 __device__ __forceinline__ int ubegin(int c, const TcPartition &p) { return (int)((long long)c * p.units / p.grid); }
 
+constexpr int RD_MAX_GRID = 160;   // CTAs (or CTA pairs) of one GEMM launch
+constexpr int RD_MAX_UROWS = 512;  // weight tiles (or tile pairs) of one launch
+
+// Per-CTA tables of a partition, so that the per-element loops need no
+// division: first[c] = first unit row of contributor c; clo/chi[u] = the
+// contributors of unit row u.
+struct RdTab {
+    int first[RD_MAX_GRID];
+    short clo[RD_MAX_UROWS], chi[RD_MAX_UROWS];
+};
+
+// (32-bit arithmetic: the launcher checks units * grid < 2^31)
+__device__ __forceinline__ void rd_build(const TcPartition &p, int n_urows, RdTab &tab)
+{
+    const unsigned g = (unsigned)p.grid, un = (unsigned)p.units, nkb = (unsigned)p.nkb;
+    for (int c = threadIdx.x; c < p.grid; c += blockDim.x)
+        tab.first[c] = (int)((unsigned)c * un / g / nkb);
+    for (int u = threadIdx.x; u < n_urows; u += blockDim.x) {
+        const unsigned u0 = (unsigned)u * nkb;
+        tab.clo[u] = (short)((u0 * g + g - 1) / un);
+        tab.chi[u] = (short)(((u0 + nkb - 1) * g + g - 1) / un);
+    }
+    __syncthreads();
+}
+
+// Sum, in contributor order, the NF (8 or 16) fp32 partials of output
+// features n0.. of token t; the loads of up to MAXC contributors are
+// issued together.
+template <int NF, int MAXC>
+__device__ __forceinline__ void rd_sum(const TcPartition &p, const RdTab &tab, int t, int n0, float (&acc)[NF])
+{
+    int ur, r, col;
+    tc_part_loc(p, t, n0 >> 7, ur, r, col);
+    const int c_lo = tab.clo[ur], c_hi = tab.chi[ur];
+#pragma unroll
+    for (int k = 0; k < NF; ++k)
+        acc[k] = 0.f;
+    for (int cb = c_lo; cb <= c_hi; cb += MAXC) {
+        float4 v[MAXC][NF / 4];
+#pragma unroll
+        for (int i = 0; i < MAXC; ++i) {
+            const int c = cb + i;
+            if (c <= c_hi) {
+                const int slot = ur - tab.first[c];
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    p.ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
+#pragma unroll
+                for (int e = 0; e < NF / 4; ++e)
+                    v[i][e] = __ldcg(src + e);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < MAXC; ++i) {
+            if (cb + i <= c_hi) {
+#pragma unroll
+                for (int e = 0; e < NF / 4; ++e) {
+                    acc[4 * e] += v[i][e].x;
+                    acc[4 * e + 1] += v[i][e].y;
+                    acc[4 * e + 2] += v[i][e].z;
+                    acc[4 * e + 3] += v[i][e].w;
+                }
+            }
+        }
+    }
+}
+
+__host__ __device__ inline int rd_urows(const TcPartition &p, int N)
+{
+    const int mt = (N + 127) / 128;
+    return p.pair ? (mt + 1) / 2 : mt;
+}
+
 __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
 {
+    __shared__ RdTab tab;
     const int t = blockIdx.x;
     const TcPartition &p = a.part;
+    rd_build(p, rd_urows(p, a.N), tab);
     float h[RN_MAX_GROUPS][8];
     float ss = 0.f;
 #pragma unroll
@@ -42,28 +116,8 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
         const int n0 = (threadIdx.x + i * RN_THREADS) * 8;
         if (n0 >= a.N)
             break;
-        int mt, r, col;
-        tc_part_loc(p, t, n0 >> 7, mt, r, col);
-        const long long u0 = (long long)mt * p.nkb;
-        const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
         float acc[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            acc[k] = 0.f;
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const int slot = mt - ubegin(c, p) / p.nkb;
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
-            const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
-            acc[0] += x0.x;
-            acc[1] += x0.y;
-            acc[2] += x0.z;
-            acc[3] += x0.w;
-            acc[4] += x1.x;
-            acc[5] += x1.y;
-            acc[6] += x1.z;
-            acc[7] += x1.w;
-        }
+        rd_sum<8, 8>(p, tab, t, n0, acc);
         const uint4 rv = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
         const bf16 *re = reinterpret_cast<const bf16 *>(&rv);
         float o[8];
@@ -105,34 +159,16 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
 // Generic finish: every 16-feature group of row t is the sum of its
 // contributors' partials, handed to the fused epilogue (RoPE + KV append
 // for the QKV projection, SwiGLU for gate/up).
-__global__ void __launch_bounds__(128) k_reduce_epi(TcPartition p, EpiParams ep)
+constexpr int RE_THREADS = 256;
+
+__global__ void __launch_bounds__(RE_THREADS) k_reduce_epi(TcPartition p, EpiParams ep)
 {
+    __shared__ RdTab tab;
     const int t = blockIdx.x;
-    {
-        const int n0 = (blockIdx.y * 128 + threadIdx.x) * 16;
-        if (n0 >= ep.N)
-            return;
-        int mt, r, col;
-        tc_part_loc(p, t, n0 >> 7, mt, r, col);
-        const long long u0 = (long long)mt * p.nkb;
-        const int c_lo = owner(u0, p), c_hi = owner(u0 + p.nkb - 1, p);
+    rd_build(p, rd_urows(p, ep.N), tab);
+    for (int n0 = threadIdx.x * 16; n0 < ep.N; n0 += RE_THREADS * 16) {
         float v[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-            v[k] = 0.f;
-        for (int c = c_lo; c <= c_hi; ++c) {
-            const int slot = mt - ubegin(c, p) / p.nkb;
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 f = __ldcg(src + e);
-                v[4 * e] += f.x;
-                v[4 * e + 1] += f.y;
-                v[4 * e + 2] += f.z;
-                v[4 * e + 3] += f.w;
-            }
-        }
+        rd_sum<16, 4>(p, tab, t, n0, v);
         epi_group(ep, t, n0, v);
     }
 }
@@ -145,8 +181,10 @@ cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cuda
         return cudaSuccess;
     if (ep.N % 16 != 0 && ep.mode != EPI_F32)  // fp32 output has a scalar tail
         return cudaErrorInvalidValue;
-    dim3 grid(ep.T, ((ep.N + 15) / 16 + 127) / 128);
-    k_reduce_epi<<<grid, 128, 0, s>>>(part, ep);
+    if (part.grid > RD_MAX_GRID || rd_urows(part, ep.N) > RD_MAX_UROWS ||
+        (long long)part.units * part.grid >= (1ll << 31))
+        return cudaErrorInvalidValue;
+    k_reduce_epi<<<ep.T, RE_THREADS, 0, s>>>(part, ep);
     return cudaGetLastError();
 }
 
@@ -156,6 +194,9 @@ cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16
     if (T <= 0)
         return cudaSuccess;
     if (N % 8 != 0 || N > RN_THREADS * 8 * RN_MAX_GROUPS)
+        return cudaErrorInvalidValue;
+    if (part.grid > RD_MAX_GRID || rd_urows(part, N) > RD_MAX_UROWS ||
+        (long long)part.units * part.grid >= (1ll << 31))
         return cudaErrorInvalidValue;
     RnArgs a{part, T, N, resid, out, gamma, norm_out, eps};
     k_reduce_norm<<<T, RN_THREADS, 0, s>>>(a);

@@ -310,6 +310,42 @@ __device__ __forceinline__ void tma_load_2d_pair_elect(void *dst, const CUtensor
         : "memory");
 }
 
+// L2 policy for data read once per pass (the weight stream): evicted
+// before anything else, so the fp32 partials written meanwhile stay in L2
+// for the pass that reduces them.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint_elect(void *dst, const CUtensorMap *m, uint32_t bar_cluster,
+                                                            int c0, int c1, uint64_t policy)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;\n"
+        "}\n" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)m), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2_hint_elect(const void *src, uint32_t bytes, uint64_t policy)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred e;\n"
+        "elect.sync _|e, 0xffffffff;\n"
+        "@e cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;\n"
+        "}\n" ::"l"((uint64_t)src),
+        "r"(bytes), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_remote_arrive(uint32_t bar_cluster)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
