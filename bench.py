@@ -218,6 +218,45 @@ def time_steps(torch, ctx, fn, steps, world):
     return e0.elapsed_time(e1)
 
 
+# ncu summaries under profiles/ that carry a measured DRAM traffic figure for
+# a kernel: "traffic_bytes_per_launch: N" and "sources: a b c" (files under
+# the package's csrc/) with "sources_sha256: H" of their concatenated bytes.
+# The figure is reported only while those sources are unchanged.
+TRAFFIC_PROFILES = {
+    "attention": "attention_llama13b_hybrid_c256_d18.md",
+    "gemm_gate_up": "gemm_pair_gate_up_llama13b_hybrid_c256_d18.md",
+}
+
+
+def sources_sha256(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "chunked_prefill_hybrid_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kind):
+    fn = TRAFFIC_PROFILES.get(kind)
+    path = os.path.join(ROOT, "profiles", fn) if fn else None
+    if not path or not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.split(":", 1)[0].strip() in ("traffic_bytes_per_launch", "sources",
+                                                                   "sources_sha256"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+    try:
+        if sources_sha256(kv["sources"].split()) != kv["sources_sha256"]:
+            return None  # the kernel changed since the counters were taken
+        return float(kv["traffic_bytes_per_launch"])
+    except (KeyError, OSError, ValueError):
+        return None
+
+
 def roofline_for(kind, prof, dims, T, D, ctx_len, pk):
     """Algorithmic bytes / flops of one launch of `kind` and its bound."""
     H, F, d = dims.hidden, dims.ffn, dims.head_dim
@@ -247,11 +286,11 @@ def roofline_for(kind, prof, dims, T, D, ctx_len, pk):
     if t_tc > t_mem:
         ach = flops / per_launch_s / 1e12
         return {"kernel": kind, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / pk["bf16_tflops"], "traffic": None, "algorithmic": flops,
+                "frac": ach / pk["bf16_tflops"], "traffic": measured_traffic(kind), "algorithmic": flops,
                 "per_launch_us": per_launch_s * 1e6, "peak_source": pk["source"] + " (burst)"}
     ach = byts / per_launch_s / 1e9
     return {"kernel": kind, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": ach / pk["hbm_gbs"], "traffic": None, "algorithmic": byts,
+            "frac": ach / pk["hbm_gbs"], "traffic": measured_traffic(kind), "algorithmic": byts,
             "per_launch_us": per_launch_s * 1e6, "peak_source": pk["source"]}
 
 

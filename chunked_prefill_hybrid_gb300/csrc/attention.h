@@ -26,6 +26,6 @@ struct AttnParams {
 int attn_smem_bytes(int head_dim);
 int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *items, int *part_off,
                      int *n_chunk_items);
-cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s);
+cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl = false);
 
 }  // namespace hb

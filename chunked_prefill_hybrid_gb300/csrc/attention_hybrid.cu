@@ -534,6 +534,8 @@ __global__ void __launch_bounds__(128) k_attention_hybrid(AttnParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    pdl_trigger();
+    pdl_wait();  // q and the batch's new K/V come from the previous kernel
     const int item = blockIdx.x / p.n_heads;
     const int head = blockIdx.x % p.n_heads;
     if (item >= p.n_items) {
@@ -588,7 +590,7 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
     return n;
 }
 
-cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s)
+cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl)
 {
     if (p.n_items <= 0)
         return cudaSuccess;
@@ -602,7 +604,10 @@ cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s)
                 return e;
             configured[1] = true;
         }
-        k_attention_hybrid<128><<<p.n_items * p.n_heads, 128, smem, s>>>(p);
+        cudaError_t e = launch_kernel(pdl, k_attention_hybrid<128>, dim3(p.n_items * p.n_heads), dim3(128),
+                                      (size_t)smem, s, p);
+        if (e != cudaSuccess)
+            return e;
     } else if (p.head_dim == 64) {
         if (!configured[0]) {
             cudaError_t e =
@@ -611,7 +616,10 @@ cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s)
                 return e;
             configured[0] = true;
         }
-        k_attention_hybrid<64><<<p.n_items * p.n_heads, 128, smem, s>>>(p);
+        cudaError_t e = launch_kernel(pdl, k_attention_hybrid<64>, dim3(p.n_items * p.n_heads), dim3(128),
+                                      (size_t)smem, s, p);
+        if (e != cudaSuccess)
+            return e;
     } else {
         return cudaErrorInvalidValue;
     }

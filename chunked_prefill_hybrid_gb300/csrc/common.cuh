@@ -42,6 +42,38 @@ struct BatchDev {
     const int *bt;         // concatenated block tables
 };
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel on
+// the stream is still running; pdl_wait() returns once that kernel has
+// finished and its writes are visible, so it must precede the first read
+// of anything the previous kernel produces.  pdl_trigger() lets the next
+// kernel be scheduled as soon as every CTA of this one has started.
+// Without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch a kernel, with the programmatic stream-serialization attribute
+// when pdl is set (the kernel must then call pdl_wait before it reads what
+// the previous kernel on the stream writes).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Epilogue of the fused GEMMs (fp32 accumulators of output pairs).
 // EPI_PARTIAL (tensor-core GEMM only): every CTA writes its fp32 partial
 // tile(s) to the workspace and a separate kernel reduces them.

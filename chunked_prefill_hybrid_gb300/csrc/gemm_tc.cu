@@ -605,6 +605,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int cta = clu * 2 + r;
     const int u0 = unit_begin(clu, a), u1 = unit_begin(clu + 1, a);
     const int rel_mask = a.rel - 1, rel_shift = a.rel == 2 ? 1 : 0;
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i)
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const SegIter seg_it(u0, u1, a.nkb);
         int it = 0, s = 0;
         uint32_t ph = 0;
-        bool ok = true;
+        bool ok = true, waited = false;
         for (int i = 0; i < seg_it.n && ok; ++i) {
             int sa, sb;
             seg_it.get(i, sa, sb);
@@ -672,6 +673,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (r == 0)
                     mbar_expect_tx_elect(&full[s], bytes);
                 tma_load_2d_pair_hint_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM, wpol);
+                if (!waited) {
+                    pdl_wait();  // the activations are the previous kernel's output
+                    waited = true;
+                }
 #pragma unroll
                 for (int sub = 0; sub < 2; ++sub)
                     if (sub < a.nsub)
@@ -1127,7 +1132,7 @@ size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, cons
 }
 
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
-                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part)
+                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part, bool pdl)
 {
     if (T <= 0)
         return cudaSuccess;
@@ -1212,6 +1217,13 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
     if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)(a.n_sub / 2)))
         return cudaErrorInvalidValue;
     cfg.gridDim = dim3((unsigned)(a.grid * 2));
+    cudaLaunchAttribute attr2[2] = {attr[0], {}};
+    if (pdl) {
+        attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr2[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr2;
+        cfg.numAttrs = 2;
+    }
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair, tmW, tmX, a, ep);
     if (e != cudaSuccess)
         return e;

@@ -74,8 +74,11 @@ size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, cons
 
 // The same product on CTA pairs with the 2-SM MMA (T <= TC_PAIR_MAX_T);
 // tmW must use 128-row boxes.
+// pdl: launch with programmatic stream serialization (the weight stream
+// starts while the previous kernel finishes; activations are read after it).
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
-                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr);
+                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr,
+                             bool pdl = false);
 
 // acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
 // tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).
@@ -86,11 +89,11 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf
 // out = bf16(resid + sum of the partial tiles of `part`) for T x N outputs;
 // if gamma: norm_out = bf16(out * rsqrt(mean(out^2) + eps) * gamma) per row.
 cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16 *resid, bf16 *out,
-                               const float *gamma, bf16 *norm_out, float eps, cudaStream_t s);
+                               const float *gamma, bf16 *norm_out, float eps, cudaStream_t s, bool pdl = false);
 
 // Finish a partial-mode GEMM: sum each (token, 16 stored features) group's
 // partials in contributor order and apply ep's fused epilogue (ep.N % 16 == 0
 // except for EPI_F32).
-cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s);
+cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s, bool pdl = false);
 
 }  // namespace hb

@@ -7,7 +7,7 @@ namespace hb {
 
 // RMSNorm: y[t][i] = bf16(x[t][i] * rsqrt(mean_i x[t][i]^2 + eps) * gamma[i]).
 cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, int H, float eps,
-                           cudaStream_t s);
+                           cudaStream_t s, bool pdl = false);
 
 // Reference SIMT GEMM: acc[t][n] = sum_k X[t][k] W[n][k], then the epilogue.
 // tiled: W is in the tensor-core layout [n/128][k/64][128][64], else [N][K].

@@ -15,6 +15,8 @@ template <int THREADS>
 __global__ void __launch_bounds__(THREADS) k_rmsnorm(const bf16 *__restrict__ x, const float *__restrict__ gamma,
                                                      bf16 *__restrict__ y, int H, float eps)
 {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const bf16 *xr = x + (size_t)t * H;
     bf16 *yr = y + (size_t)t * H;
@@ -55,12 +57,13 @@ __global__ void __launch_bounds__(THREADS) k_rmsnorm(const bf16 *__restrict__ x,
     }
 }
 
-cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, int H, float eps, cudaStream_t s)
+cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, int H, float eps, cudaStream_t s,
+                           bool pdl)
 {
     if (T <= 0)
         return cudaSuccess;
-    k_rmsnorm<256><<<T, 256, 0, s>>>(x, gamma, y, H, eps);
-    return cudaGetLastError();
+    cudaError_t e = launch_kernel(pdl, k_rmsnorm<256>, dim3(T), dim3(256), 0, s, x, gamma, y, H, eps);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------- reference GEMM

@@ -167,7 +167,7 @@ static cudaError_t launch_tc(const hb_ctx *ctx, const LayerMaps &M, int kind, co
                              int N, int K, const EpiParams &ep, TcPartition *part = nullptr)
 {
     if (ctx->gemm_impl == 2)
-        return launch_gemm_pair(M.m[kind][0], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part);
+        return launch_gemm_pair(M.m[kind][0], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part, true);
     return launch_gemm_tc(M.get(kind, T), W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part);
 }
 
@@ -222,7 +222,7 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
         TcPartition part;
         cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, pp, &part);
         if (e == cudaSuccess)
-            e = launch_reduce_epi(part, er, ctx->stream);
+            e = launch_reduce_epi(part, er, ctx->stream, true);
         if (e != cudaSuccess)
             return e;
     }
@@ -247,7 +247,7 @@ static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const 
         if (e != cudaSuccess)
             return e;
         e = launch_reduce_norm(part, Tn, N, resid + (size_t)t0 * N, out + (size_t)t0 * N, gamma,
-                               norm_out + (size_t)t0 * N, c.rms_eps, ctx->stream);
+                               norm_out + (size_t)t0 * N, c.rms_eps, ctx->stream, ctx->gemm_impl == 2);
         if (e != cudaSuccess)
             return e;
         *launches += 2;
@@ -274,7 +274,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     // on the tensor-core path norm-1 of every layer but the first was
     // produced by the previous layer's final reduce
     if (!tc || l == l_first)
-        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s));
+        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s, ctx->gemm_impl == 2));
 
     EpiParams ep{};
     ep.mode = EPI_QKV;
@@ -311,7 +311,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
         ap.part = f->attn_part;
         ap.counters = f->attn_counters;
         ap.err = ctx->err_word;
-        LK(K_ATTENTION, launch_attention_hybrid(ap, s));
+        LK(K_ATTENTION, launch_attention_hybrid(ap, s, ctx->gemm_impl == 2));
     } else {
         LK(K_ATTENTION,
            launch_attention_simple(ctx->q, L.k_pool, L.v_pool, b, c.n_heads, c.n_kv_heads, d, ctx->attn_o, s));

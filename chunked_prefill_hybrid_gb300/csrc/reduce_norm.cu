@@ -106,9 +106,11 @@ __host__ __device__ inline int rd_urows(const TcPartition &p, int N)
 __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
 {
     __shared__ RdTab tab;
+    pdl_trigger();
     const int t = blockIdx.x;
     const TcPartition &p = a.part;
     rd_build(p, rd_urows(p, a.N), tab);
+    pdl_wait();
     float h[RN_MAX_GROUPS][8];
     float ss = 0.f;
 #pragma unroll
@@ -164,8 +166,10 @@ constexpr int RE_THREADS = 256;
 __global__ void __launch_bounds__(RE_THREADS) k_reduce_epi(TcPartition p, EpiParams ep)
 {
     __shared__ RdTab tab;
+    pdl_trigger();
     const int t = blockIdx.x;
     rd_build(p, rd_urows(p, ep.N), tab);
+    pdl_wait();
     for (int n0 = threadIdx.x * 16; n0 < ep.N; n0 += RE_THREADS * 16) {
         float v[16];
         rd_sum<16, 4>(p, tab, t, n0, v);
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(RE_THREADS) k_reduce_epi(TcPartition p, EpiPar
 
 }  // namespace
 
-cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s)
+cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cudaStream_t s, bool pdl)
 {
     if (ep.T <= 0)
         return cudaSuccess;
@@ -184,12 +188,12 @@ cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cuda
     if (part.grid > RD_MAX_GRID || rd_urows(part, ep.N) > RD_MAX_UROWS ||
         (long long)part.units * part.grid >= (1ll << 31))
         return cudaErrorInvalidValue;
-    k_reduce_epi<<<ep.T, RE_THREADS, 0, s>>>(part, ep);
-    return cudaGetLastError();
+    cudaError_t e = launch_kernel(pdl, k_reduce_epi, dim3(ep.T), dim3(RE_THREADS), 0, s, part, ep);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16 *resid, bf16 *out, const float *gamma,
-                               bf16 *norm_out, float eps, cudaStream_t s)
+                               bf16 *norm_out, float eps, cudaStream_t s, bool pdl)
 {
     if (T <= 0)
         return cudaSuccess;
@@ -199,8 +203,8 @@ cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16
         (long long)part.units * part.grid >= (1ll << 31))
         return cudaErrorInvalidValue;
     RnArgs a{part, T, N, resid, out, gamma, norm_out, eps};
-    k_reduce_norm<<<T, RN_THREADS, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaError_t e = launch_kernel(pdl, k_reduce_norm, dim3(T), dim3(RN_THREADS), 0, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace hb
