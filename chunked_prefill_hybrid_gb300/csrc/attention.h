@@ -5,9 +5,23 @@
 
 namespace hb {
 
-// Keys per decode split; the split count of a decode depends on its context
-// length only, so a decode's result does not depend on the rest of the batch.
-constexpr int ATTN_SPLIT = 256;
+// Decode splits: a decode with n keys runs as max(1, n / ATTN_SPLIT) splits
+// of near-equal length (so every split has ATTN_SPLIT..2*ATTN_SPLIT-1 keys).
+// The split count depends on the context length only, so a decode's result
+// does not depend on the rest of the batch.
+constexpr int ATTN_SPLIT = 1024;
+// Keys per split (a multiple of 16) and the number of splits; every split
+// is non-empty.
+__host__ __device__ inline int attn_split_len(int nkeys)
+{
+    const int n = nkeys / ATTN_SPLIT > 1 ? nkeys / ATTN_SPLIT : 1;
+    return ((nkeys + n - 1) / n + 15) & ~15;
+}
+__host__ __device__ inline int attn_n_splits(int nkeys)
+{
+    const int len = attn_split_len(nkeys);
+    return (nkeys + len - 1) / len;
+}
 
 struct AttnParams {
     BatchDev b;

@@ -16,9 +16,10 @@
 //               accumulate), online softmax in registers.  P is split into
 //               bf16 hi + lo parts for the PV product so the weights keep
 //               ~16 significant bits.
-//   decode split one head of a single-row sequence over a range of at most
-//               256 keys.  Each 16-token block of K and of V is one contiguous
-//               4 KB run in the pool and is streamed with cp.async.bulk into
+//   decode split one head of a single-row sequence over a range of its keys
+//               (1024..2047 keys; shorter contexts are one split).  Each
+//               16-token block of K and of V is one contiguous 4 KB run in
+//               the pool and is streamed with cp.async.bulk into
 //               an 8-stage shared-memory ring (mbarrier pipeline); 4 warps
 //               each take 4 tokens of a block, warp-shuffle dot products and
 //               an online softmax per warp.  The number of splits depends on
@@ -298,9 +299,8 @@ __device__ __forceinline__ int rs_token_of(int lane)
 // are near-equal, 16-aligned, and depend on nkeys alone.
 __device__ __forceinline__ void split_range(int nkeys, int split, int &k0, int &k1, int &n_splits)
 {
-    n_splits = (nkeys + ATTN_SPLIT - 1) / ATTN_SPLIT;
-    int len = (nkeys + n_splits - 1) / n_splits;
-    len = (len + 15) & ~15;
+    n_splits = attn_n_splits(nkeys);
+    const int len = attn_split_len(nkeys);
     k0 = split * len;
     k1 = min(nkeys, k0 + len);
 }
@@ -355,7 +355,7 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
         const bf16 *qr = p.q + ((size_t)row * p.n_heads + head) * D + lane * E;
 #pragma unroll
         for (int i = 0; i < E; ++i) {
-            qv[i] = bf2f(qr[i]) * sl2;
+            qv[i] = bf2f(__ushort_as_bfloat16(__ldcg(reinterpret_cast<const unsigned short *>(qr + i)))) * sl2;
             acc[i] = 0.f;
         }
     }
@@ -529,35 +529,57 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
         p.counters[seq * p.n_heads + head] = 0;
 }
 
+// Chunk tiles and decode splits run as two kernels so that each gets the
+// registers and shared memory it needs (the decode splits fit three CTAs on
+// an SM beside a chunk tile) and the two overlap: the chunk kernel waits for
+// the QKV projection, then lets the decode kernel start; the decode kernel
+// reads q and the pool without a wait of its own (through L2 only, never
+// L1), and its last CTA waits for the chunk kernel before exiting, so the
+// next kernel, which waits for the decode kernel, sees both.
 template <int D>
-__global__ void __launch_bounds__(128) k_attention_hybrid(AttnParams p)
+__global__ void __launch_bounds__(128) k_attention_chunk(AttnParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    pdl_trigger();
     pdl_wait();  // q and the batch's new K/V come from the previous kernel
+    pdl_trigger();
     const int item = blockIdx.x / p.n_heads;
     const int head = blockIdx.x % p.n_heads;
-    if (item >= p.n_items) {
+    if (item >= p.n_chunk_items) {
         if (threadIdx.x == 0)
             set_dev_err(p.err, DERR_BAD_WORK);
         return;
     }
-    const int seq = p.items[2 * item];
-    const int arg = p.items[2 * item + 1];
-    if (item < p.n_chunk_items)
-        chunk_tile<D>(p, seq, head, arg, smem);
-    else
-        decode_split<D>(p, seq, head, arg, smem);
+    chunk_tile<D>(p, p.items[2 * item], head, p.items[2 * item + 1], smem);
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) k_attention_decode(AttnParams p, int wait_first)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    if (wait_first)
+        pdl_wait();  // launched right after the QKV projection
+    pdl_trigger();
+    const int item = p.n_chunk_items + blockIdx.x / p.n_heads;
+    const int head = blockIdx.x % p.n_heads;
+    if (item < p.n_items)
+        decode_split<D>(p, p.items[2 * item], head, p.items[2 * item + 1], smem);
+    else if (threadIdx.x == 0)
+        set_dev_err(p.err, DERR_BAD_WORK);
+    if (!wait_first && blockIdx.x == gridDim.x - 1)
+        pdl_wait();  // the grid completes only after the chunk kernel
 }
 
 }  // namespace
 
+static int chunk_smem_bytes(int D) { return CQ * 2 * D + 4 * CK * 2 * D + 1024; }  // Q + 2 x (K, V)
+static int decode_smem_bytes(int D) { return NSTAGE * 64 * D + NSTAGE * 8 + 16 + 4 * (2 + D) * 4 + 1024; }
+
 int attn_smem_bytes(int D)
 {
-    const int chunk = CQ * 2 * D + 4 * CK * 2 * D;                       // Q + 2 x (K, V)
-    const int dec = NSTAGE * 64 * D + NSTAGE * 8 + 16 + 4 * (2 + D) * 4;
-    return (chunk > dec ? chunk : dec) + 1024;
+    const int c = chunk_smem_bytes(D), d = decode_smem_bytes(D);
+    return c > d ? c : d;
 }
 
 // Work list: chunk tiles (64 rows) of every sequence with more than one row,
@@ -578,7 +600,7 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
     for (int s = 0; s < n_seq; ++s) {
         part_off[s] = off;
         if (seq_nq[s] == 1) {
-            const int ns = (seq_pos0[s] + 1 + ATTN_SPLIT - 1) / ATTN_SPLIT;
+            const int ns = attn_n_splits(seq_pos0[s] + 1);
             for (int sp = 0; sp < ns; ++sp) {
                 items[2 * n] = s;
                 items[2 * n + 1] = sp;
@@ -590,40 +612,47 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
     return n;
 }
 
+template <int D>
+static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool pdl)
+{
+    static bool configured = false;
+    const int cs = chunk_smem_bytes(D), ds = decode_smem_bytes(D);
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k_attention_chunk<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, cs);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_attention_decode<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, ds);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    const int n_dec = p.n_items - p.n_chunk_items;
+    if (p.n_chunk_items > 0) {
+        cudaError_t e = launch_kernel(pdl, k_attention_chunk<D>, dim3(p.n_chunk_items * p.n_heads), dim3(128),
+                                      (size_t)cs, s, p);
+        if (e != cudaSuccess)
+            return e;
+    }
+    if (n_dec > 0) {
+        // after a chunk kernel the decode kernel starts as its dependent and
+        // waits at its end; alone, it waits for the QKV projection first
+        const int wait_first = (p.n_chunk_items > 0 && pdl) ? 0 : 1;
+        cudaError_t e = launch_kernel(pdl, k_attention_decode<D>, dim3(n_dec * p.n_heads), dim3(128), (size_t)ds, s,
+                                      p, wait_first);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl)
 {
     if (p.n_items <= 0)
         return cudaSuccess;
-    const int smem = attn_smem_bytes(p.head_dim);
-    static bool configured[2] = {false, false};
-    if (p.head_dim == 128) {
-        if (!configured[1]) {
-            cudaError_t e =
-                cudaFuncSetAttribute(k_attention_hybrid<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess)
-                return e;
-            configured[1] = true;
-        }
-        cudaError_t e = launch_kernel(pdl, k_attention_hybrid<128>, dim3(p.n_items * p.n_heads), dim3(128),
-                                      (size_t)smem, s, p);
-        if (e != cudaSuccess)
-            return e;
-    } else if (p.head_dim == 64) {
-        if (!configured[0]) {
-            cudaError_t e =
-                cudaFuncSetAttribute(k_attention_hybrid<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-            if (e != cudaSuccess)
-                return e;
-            configured[0] = true;
-        }
-        cudaError_t e = launch_kernel(pdl, k_attention_hybrid<64>, dim3(p.n_items * p.n_heads), dim3(128),
-                                      (size_t)smem, s, p);
-        if (e != cudaSuccess)
-            return e;
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (p.head_dim == 128)
+        return launch_attention_d<128>(p, s, pdl);
+    if (p.head_dim == 64)
+        return launch_attention_d<64>(p, s, pdl);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace hb

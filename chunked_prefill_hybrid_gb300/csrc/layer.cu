@@ -44,7 +44,7 @@ struct FastPath {
 };
 
 static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + 1; }
-static size_t max_splits_per_seq(const hb_model_config &c) { return ((size_t)c.max_pos + ATTN_SPLIT - 1) / ATTN_SPLIT; }
+static size_t max_splits_per_seq(const hb_model_config &c) { return (size_t)(c.max_pos + 1) / ATTN_SPLIT + 1; }
 static size_t max_items(const hb_model_config &c)
 {
     return ((size_t)c.max_tokens + 63) / 64 + max_seqs(c) * max_splits_per_seq(c);

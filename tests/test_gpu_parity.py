@@ -117,12 +117,14 @@ def test_tiny_edge_cases(case, kern):
     ctx.free()
 
 
-@pytest.mark.parametrize("kern", ["tc+hybrid", "simt+hybrid"])
+@pytest.mark.parametrize("kern", ["pair+hybrid", "tc+hybrid", "simt+hybrid"])
 @pytest.mark.parametrize("dims", [D128, GQA], ids=["d128", "gqa"])
 @pytest.mark.parametrize("case", [
     ("hybrid", 200, 130, [0, 63, 64, 255, 256, 300, 1000]),
     ("prefill_only", 0, 257, []),
     ("decode_only", None, 0, [5, 511, 512, 513]),
+    # contexts of 2048 keys and more run as several decode splits, merged
+    ("split_decodes", 64, 40, [2046, 2047, 2048, 3100, 4500]),
 ])
 def test_head_dim_and_gqa_cases(case, dims, kern):
     name, off, ln, ctxs = case
