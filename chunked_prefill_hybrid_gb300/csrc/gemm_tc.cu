@@ -76,8 +76,10 @@ struct TcArgs {
 // that the stream-K fixups of split tiles overlap the remaining work.
 // Distance (k-blocks of 16 KB) the weight stream is prefetched into L2 ahead
 // of its TMA loads; the loads then find their data in L2, so fewer shared-
-// memory stages cover the HBM latency.
-constexpr int TC_PREFETCH = 12;
+// memory stages cover the HBM latency.  (Measured on the layer step: 4 beats
+// both no prefetch and deeper ones, which only add requests once the weight
+// stream is marked evict-first.)
+constexpr int TC_PREFETCH = 4;
 
 struct SegIter {
     int u0, u1, nkb, n;
