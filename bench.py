@@ -53,57 +53,111 @@ def peaks():
 # --------------------------------------------------------------- clocks
 
 class Clocks:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled during the timed region.
+
+    Polls NVML (the driver's libnvidia-ml, through ctypes) about every
+    millisecond from a thread, so even a timed region of a few milliseconds
+    gets samples; falls back to nvidia-smi at 200 ms when NVML is missing."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+        self.samples = []
+        self.max_mhz = None
+        self.nvml = None
+        self.handle = None
+        self.thread = None
+        self.stop = False
+        self.smi = None
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(self.gpu)
+            bus = "%08x:%02x:%02x.0" % (getattr(pr, "pci_domain_id", 0), pr.pci_bus_id, pr.pci_device_id)
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.gpu, ctypes.byref(h)) != 0:
+            return False
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self.nvml, self.handle = lib, h
+        return True
+
+    def _poll(self):
+        import ctypes
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_r = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop:
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0 and \
+                    get_r(self.handle, ctypes.byref(rs)) == 0:
+                self.samples.append((float(mhz.value), int(rs.value)))
+            time.sleep(0.001)
 
     def __enter__(self):
+        import threading
+        if self._open_nvml():
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self.smi = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={q}",
+                                         "--format=csv,noheader,nounits", "-lms", "200"],
+                                        stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
-            self.proc = None
+            self.smi = None
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
+        self.stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        if self.smi is not None:
+            self.smi.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self.smi.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-
-    def summary(self):
-        rows = []
-        try:
-            with open(self.path) as f:
-                for line in f:
-                    parts = [t.strip() for t in line.split(",")]
-                    if len(parts) >= 9:
-                        rows.append(parts)
-        except OSError:
-            pass
-        finally:
+                self.smi.kill()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            bits = [0x8, 0x40, 0x20, 0x4]
             try:
+                with open(self.path) as f:
+                    for line in f:
+                        t = [x.strip() for x in line.split(",")]
+                        if len(t) >= 6 and t[0].replace(".", "").isdigit():
+                            r = sum(b for b, v in zip(bits, t[2:6]) if v.lower().startswith("active"))
+                            self.samples.append((float(t[0]), r))
+                            if t[1].replace(".", "").isdigit():
+                                self.max_mhz = float(t[1])
                 os.unlink(self.path)
             except OSError:
                 pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 # ----------------------------------------------------------- distributed
@@ -297,7 +351,7 @@ def roofline_for(kind, prof, dims, T, D, ctx_len, pk):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=10.0)
