@@ -1,6 +1,8 @@
 // attention.h -- host interface of the hybrid paged-attention kernel.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace hb {
@@ -38,8 +40,19 @@ struct AttnParams {
 };
 
 int attn_smem_bytes(int head_dim);
+// Work list: chunk tiles of chunk_rows rows (64 for the mma.sync kernel,
+// attn_tc_chunk_rows() for the tcgen05 one), then the decode splits.
 int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *items, int *part_off,
-                     int *n_chunk_items);
-cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl = false);
+                     int *n_chunk_items, int chunk_rows = 64);
+// Chunk tiles (mma.sync kernel, unless skip_chunk) then decode splits.
+// With skip_chunk the decode kernel follows a chunk kernel launched just
+// before it (launch_attention_chunk_tc).
+cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl = false, bool skip_chunk = false);
+
+// The chunk's attention on the tcgen05 tensor cores (attention_tc.cu):
+// 128-row tiles; tmK / tmV: make_tmap_kv_pool maps of the layer's pools.
+int attn_tc_chunk_rows();
+cudaError_t launch_attention_chunk_tc(const AttnParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                      cudaStream_t s, bool pdl);
 
 }  // namespace hb

@@ -585,12 +585,13 @@ int attn_smem_bytes(int D)
 // Work list: chunk tiles (64 rows) of every sequence with more than one row,
 // then the splits of every single-row sequence.  items: [n_items][2] = (seq,
 // q0 or split); part_off: [n_seq] first partial slot of each sequence.
-int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *items, int *part_off, int *n_chunk_items)
+int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *items, int *part_off, int *n_chunk_items,
+                     int chunk_rows)
 {
     int n = 0;
     for (int s = 0; s < n_seq; ++s)
         if (seq_nq[s] > 1)
-            for (int q0 = 0; q0 < seq_nq[s]; q0 += CQ) {
+            for (int q0 = 0; q0 < seq_nq[s]; q0 += chunk_rows) {
                 items[2 * n] = s;
                 items[2 * n + 1] = q0;
                 ++n;
@@ -613,7 +614,7 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
 }
 
 template <int D>
-static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool pdl)
+static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool pdl, bool skip_chunk)
 {
     static bool configured = false;
     const int cs = chunk_smem_bytes(D), ds = decode_smem_bytes(D);
@@ -626,7 +627,7 @@ static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool 
         configured = true;
     }
     const int n_dec = p.n_items - p.n_chunk_items;
-    if (p.n_chunk_items > 0) {
+    if (p.n_chunk_items > 0 && !skip_chunk) {
         cudaError_t e = launch_kernel(pdl, k_attention_chunk<D>, dim3(p.n_chunk_items * p.n_heads), dim3(128),
                                       (size_t)cs, s, p);
         if (e != cudaSuccess)
@@ -644,14 +645,14 @@ static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool 
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl)
+cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl, bool skip_chunk)
 {
     if (p.n_items <= 0)
         return cudaSuccess;
     if (p.head_dim == 128)
-        return launch_attention_d<128>(p, s, pdl);
+        return launch_attention_d<128>(p, s, pdl, skip_chunk);
     if (p.head_dim == 64)
-        return launch_attention_d<64>(p, s, pdl);
+        return launch_attention_d<64>(p, s, pdl, skip_chunk);
     return cudaErrorInvalidValue;
 }
 

@@ -954,6 +954,15 @@ int tc_weight_box_rows(int T)
     return G > 1 ? piece : TC_BM;
 }
 
+// The paged K or V pool [num_blocks][n_kv][16][d] as a 2D tensor of
+// num_blocks * n_kv * 16 rows of d elements, in boxes of 16 rows x 64
+// elements (128-byte swizzle): one box is half (d = 128) or all (d = 64) of
+// one head's 16-token block.
+bool make_tmap_kv_pool(CUtensorMap *m, const void *pool, int num_blocks, int n_kv, int d)
+{
+    return encode_2d(m, pool, (uint64_t)d, (uint64_t)num_blocks * n_kv * 16, (uint64_t)d * 2, 64, 16);
+}
+
 // G = ceil(T / 256) equal token groups of n_sub (a multiple of 16) columns,
 // one MMA of N = n_sub per k-block and two TMEM accumulators per CTA, so
 // the epilogue of one tile overlaps the main loop of the next.  (The kernel

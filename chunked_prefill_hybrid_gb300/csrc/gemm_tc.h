@@ -63,6 +63,8 @@ size_t tiled_weight_elems(int N, int K);
 // mode 0: rows as given; 1: RoPE pair permutation within heads of `a` rows;
 // 2: gate/up interleave (gate rows 0..a-1, up rows a..2a-1 of src).
 cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mode, int a, cudaStream_t s);
+// The paged K or V pool as a TMA map of 16-row x 64-element boxes.
+bool make_tmap_kv_pool(CUtensorMap *m, const void *pool, int num_blocks, int n_kv, int d);
 // box_rows: 128, or the multicast slice of tc_weight_box_rows(T).
 bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, int box_rows);
 int tc_weight_box_rows(int T);

@@ -41,6 +41,7 @@ struct FastPath {
     std::vector<int> items, part_off;
     const int *d_items = nullptr, *d_part_off = nullptr;
     int n_items = 0, n_chunk_items = 0;
+    std::vector<CUtensorMap> kv_maps;  // [layer][K, V] pool maps of the tcgen05 chunk attention
 };
 
 static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + 1; }
@@ -109,6 +110,12 @@ int hb_init_fast_path(hb_ctx *ctx)
                 return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
         }
     }
+    f->kv_maps.resize(2 * (size_t)c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l)
+        if (!make_tmap_kv_pool(&f->kv_maps[2 * l], ctx->layers[l].k_pool, c.num_blocks, c.n_kv_heads, c.head_dim) ||
+            !make_tmap_kv_pool(&f->kv_maps[2 * l + 1], ctx->layers[l].v_pool, c.num_blocks, c.n_kv_heads,
+                               c.head_dim))
+            return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed for a KV pool");
     ctx->gemm_impl = 2;
     ctx->attn_impl = 1;
     return HB_OK;
@@ -134,7 +141,7 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
     FastPath *f = ctx->fast;
     int n_chunk = 0;
     const int n = attn_build_items(p.seq_nq.data(), p.seq_pos0.data(), p.n_seq, f->items.data(),
-                                   f->part_off.data(), &n_chunk);
+                                   f->part_off.data(), &n_chunk, ctx->attn_impl == 2 ? attn_tc_chunk_rows() : 64);
     if ((size_t)n > max_items(ctx->cfg))
         return ctx->set_error(HB_ERANGE, "attention work list overflow");
     std::copy(f->items.begin(), f->items.begin() + 2 * n, hm + at);
@@ -195,6 +202,17 @@ static EpiParams epi_rows(const EpiParams &ep, int t0, int Tn)
 
 // W is in the tiled layout; tmW its tensor map (for a slab of kSlab rows
 // when T is larger: the weight slice height depends on the slab's rows).
+// Attention with the tcgen05 chunk kernel, then the decode kernel as its
+// dependent (see attention.h).
+static cudaError_t launch_attention_tc(const AttnParams &ap, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                       cudaStream_t s, bool pdl)
+{
+    cudaError_t e = launch_attention_chunk_tc(ap, tmK, tmV, s, pdl);
+    if (e != cudaSuccess)
+        return e;
+    return launch_attention_hybrid(ap, s, pdl, true);
+}
+
 static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X, const bf16 *W, int T, int N, int K,
                         const EpiParams &ep)
 {
@@ -293,7 +311,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     ep.err = ctx->err_word;
     LK(K_GEMM_QKV, gemm(ctx, M, W_QKV, ctx->xn, L.w_qkv, T, ctx->n_qkv, H, ep));
 
-    if (ctx->attn_impl == 1) {
+    if (ctx->attn_impl >= 1) {
         const FastPath *f = ctx->fast;
         AttnParams ap;
         ap.b = b;
@@ -311,7 +329,11 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
         ap.part = f->attn_part;
         ap.counters = f->attn_counters;
         ap.err = ctx->err_word;
-        LK(K_ATTENTION, launch_attention_hybrid(ap, s, ctx->gemm_impl == 2));
+        const bool pdl = ctx->gemm_impl == 2;
+        if (ctx->attn_impl == 2)
+            LK(K_ATTENTION, launch_attention_tc(ap, f->kv_maps[2 * l], f->kv_maps[2 * l + 1], s, pdl));
+        else
+            LK(K_ATTENTION, launch_attention_hybrid(ap, s, pdl));
     } else {
         LK(K_ATTENTION,
            launch_attention_simple(ctx->q, L.k_pool, L.v_pool, b, c.n_heads, c.n_kv_heads, d, ctx->attn_o, s));
@@ -415,8 +437,8 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
 {
     if (!ctx)
         return HB_EINVAL;
-    if (gemm_impl < 0 || gemm_impl > 2 || attn_impl < 0 || attn_impl > 1)
-        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0, 1 or 2 and attn_impl 0 or 1");
+    if (gemm_impl < 0 || gemm_impl > 2 || attn_impl < 0 || attn_impl > 2)
+        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl and attn_impl must be 0, 1 or 2");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
     return HB_OK;

@@ -12,8 +12,6 @@ namespace hb {
 
 namespace {
 
-constexpr int RN_THREADS = 256;
-constexpr int RN_MAX_GROUPS = 4;  // hidden <= 256 * 8 * 4 = 8192
 
 struct RnArgs {
     TcPartition part;
@@ -24,12 +22,6 @@ struct RnArgs {
     bf16 *norm_out;
     float eps;
 };
-
-__device__ __forceinline__ int owner(long long u, const TcPartition &p)
-{
-    return (int)((u * p.grid + p.grid - 1) / p.units);
-}
-__device__ __forceinline__ int ubegin(int c, const TcPartition &p) { return (int)((long long)c * p.units / p.grid); }
 
 constexpr int RD_MAX_GRID = 160;   // CTAs (or CTA pairs) of one GEMM launch
 constexpr int RD_MAX_UROWS = 512;  // weight tiles (or tile pairs) of one launch
@@ -103,37 +95,34 @@ __host__ __device__ inline int rd_urows(const TcPartition &p, int N)
     return p.pair ? (mt + 1) / 2 : mt;
 }
 
-__global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
+// One thread per 8-feature group of the row (blockDim = groups rounded up
+// to whole warps, at most 1024 = hidden 8192).
+__global__ void __launch_bounds__(1024) k_reduce_norm(RnArgs a)
 {
     __shared__ RdTab tab;
+    __shared__ float red[32];
     pdl_trigger();
     const int t = blockIdx.x;
     const TcPartition &p = a.part;
     rd_build(p, rd_urows(p, a.N), tab);
     pdl_wait();
-    float h[RN_MAX_GROUPS][8];
+    const int n0 = threadIdx.x * 8;
+    float o[8];
     float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < RN_MAX_GROUPS; ++i) {
-        const int n0 = (threadIdx.x + i * RN_THREADS) * 8;
-        if (n0 >= a.N)
-            break;
+    if (n0 < a.N) {
         float acc[8];
-        rd_sum<8, 8>(p, tab, t, n0, acc);
+        rd_sum<8, 4>(p, tab, t, n0, acc);
         const uint4 rv = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
         const bf16 *re = reinterpret_cast<const bf16 *>(&rv);
-        float o[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             o[k] = bf2f(f2bf(bf2f(re[k]) + acc[k]));  // the stored bf16 value
-            h[i][k] = o[k];
             ss += o[k] * o[k];
         }
         *reinterpret_cast<uint4 *>(a.out + (size_t)t * a.N + n0) = pack8_bf16(o);
     }
     if (!a.gamma)
         return;
-    __shared__ float red[RN_THREADS / 32];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -141,19 +130,13 @@ __global__ void __launch_bounds__(RN_THREADS) k_reduce_norm(RnArgs a)
         red[threadIdx.x >> 5] = ss;
     __syncthreads();
     float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < RN_THREADS / 32; ++w)
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
         tot += red[w];
     const float rs = rsqrtf(tot / (float)a.N + a.eps);
-#pragma unroll
-    for (int i = 0; i < RN_MAX_GROUPS; ++i) {
-        const int n0 = (threadIdx.x + i * RN_THREADS) * 8;
-        if (n0 >= a.N)
-            break;
-        float o[8];
+    if (n0 < a.N) {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            o[k] = h[i][k] * rs * a.gamma[n0 + k];
+            o[k] = o[k] * rs * a.gamma[n0 + k];
         *reinterpret_cast<uint4 *>(a.norm_out + (size_t)t * a.N + n0) = pack8_bf16(o);
     }
 }
@@ -170,7 +153,9 @@ __global__ void __launch_bounds__(RE_THREADS) k_reduce_epi(TcPartition p, EpiPar
     const int t = blockIdx.x;
     rd_build(p, rd_urows(p, ep.N), tab);
     pdl_wait();
-    for (int n0 = threadIdx.x * 16; n0 < ep.N; n0 += RE_THREADS * 16) {
+    // one 16-feature group per thread; blockIdx.y picks the row's slice
+    const int n0 = (blockIdx.y * RE_THREADS + threadIdx.x) * 16;
+    if (n0 < ep.N) {
         float v[16];
         rd_sum<16, 4>(p, tab, t, n0, v);
         epi_group(ep, t, n0, v);
@@ -188,7 +173,8 @@ cudaError_t launch_reduce_epi(const TcPartition &part, const EpiParams &ep, cuda
     if (part.grid > RD_MAX_GRID || rd_urows(part, ep.N) > RD_MAX_UROWS ||
         (long long)part.units * part.grid >= (1ll << 31))
         return cudaErrorInvalidValue;
-    cudaError_t e = launch_kernel(pdl, k_reduce_epi, dim3(ep.T), dim3(RE_THREADS), 0, s, part, ep);
+    const int slices = ((ep.N + 15) / 16 + RE_THREADS - 1) / RE_THREADS;
+    cudaError_t e = launch_kernel(pdl, k_reduce_epi, dim3(ep.T, slices), dim3(RE_THREADS), 0, s, part, ep);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -197,13 +183,14 @@ cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16
 {
     if (T <= 0)
         return cudaSuccess;
-    if (N % 8 != 0 || N > RN_THREADS * 8 * RN_MAX_GROUPS)
+    if (N % 8 != 0 || N > 8 * 1024)
         return cudaErrorInvalidValue;
     if (part.grid > RD_MAX_GRID || rd_urows(part, N) > RD_MAX_UROWS ||
         (long long)part.units * part.grid >= (1ll << 31))
         return cudaErrorInvalidValue;
     RnArgs a{part, T, N, resid, out, gamma, norm_out, eps};
-    cudaError_t e = launch_kernel(pdl, k_reduce_norm, dim3(T), dim3(RN_THREADS), 0, s, a);
+    const int threads = ((N / 8) + 31) / 32 * 32;
+    cudaError_t e = launch_kernel(pdl, k_reduce_norm, dim3(T), dim3(threads), 0, s, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

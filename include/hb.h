@@ -183,8 +183,9 @@ int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int 
 /* Test hook: choose the kernels later calls use.  gemm_impl 0 = reference
  * SIMT GEMM, 1 = tcgen05 GEMM on clusters of token groups, 2 = tcgen05 GEMM
  * on CTA pairs with the 2-SM MMA (default); attn_impl 0 = one CTA per
- * (row, head), 1 = the paged hybrid-attention kernel (default).  Every
- * setting computes the same function. */
+ * (row, head), 1 = paged attention with mma.sync chunk tiles (default), 2 =
+ * paged attention with tcgen05 chunk tiles.  Every setting computes the same
+ * function. */
 int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl);
 
 /* Test hook: copy an intermediate of the LAST layer run by the latest

@@ -74,7 +74,8 @@ def check_kv(ctx, w, pools, layer=0):
 # head_dim 128 and grouped-query shapes at a size the oracle finishes quickly
 D128 = synth.ModelDims(hidden=256, n_heads=2, n_kv_heads=2, head_dim=128, ffn=512)
 GQA = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn=384)
-KERNELS = {"pair+hybrid": (2, 1), "tc+hybrid": (1, 1), "tc+simple": (1, 0), "simt+hybrid": (0, 1)}
+KERNELS = {"pair+tcattn": (2, 2), "pair+hybrid": (2, 1), "tc+hybrid": (1, 1), "tc+simple": (1, 0),
+           "simt+hybrid": (0, 1)}
 
 
 def _tiny(seed, chunk_offset, chunk_len, ctxs, n_layers=1, gamma="ones", dims=synth.TINY):
@@ -117,7 +118,7 @@ def test_tiny_edge_cases(case, kern):
     ctx.free()
 
 
-@pytest.mark.parametrize("kern", ["pair+hybrid", "tc+hybrid", "simt+hybrid"])
+@pytest.mark.parametrize("kern", ["pair+tcattn", "pair+hybrid", "tc+hybrid", "simt+hybrid"])
 @pytest.mark.parametrize("dims", [D128, GQA], ids=["d128", "gqa"])
 @pytest.mark.parametrize("case", [
     ("hybrid", 200, 130, [0, 63, 64, 255, 256, 300, 1000]),
