@@ -1142,6 +1142,13 @@ size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, cons
     return need;
 }
 
+bool tc_pair_data_parallel(const TcRuntime &rt, int N)
+{
+    const int n_mpairs = ((N + TC_BM - 1) / TC_BM + 1) / 2;
+    const int pairs = rt.num_sms / 2;
+    return n_mpairs <= pairs && 10 * n_mpairs >= 6 * pairs;
+}
+
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
                              const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part, bool pdl)
 {
@@ -1208,6 +1215,13 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         mc = n < rt.num_sms / 2 ? n : rt.num_sms / 2;
     }
     a.grid = tc_grid(units, mc);
+    if (ep.mode != EPI_PARTIAL) {
+        // data-parallel: one whole weight-tile pair per CTA pair, fused
+        // epilogue, no partials
+        if (n_mpairs > mc)
+            return cudaErrorInvalidValue;
+        a.grid = n_mpairs;
+    }
     a.slots = tc_slots(units, a.grid, a.nkb);
     if ((size_t)a.grid * 2 * a.slots * a.tg * TC_BM > rt.ws_floats)
         return cudaErrorInvalidValue;

@@ -75,7 +75,11 @@ TcShape tc_pair_shape(int T);
 size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes);
 
 // The same product on CTA pairs with the 2-SM MMA (T <= TC_PAIR_MAX_T);
-// tmW must use 128-row boxes.
+// tmW must use 128-row boxes.  With ep.mode EPI_PARTIAL the work is split
+// stream-K and every CTA leaves fp32 partials (part says where); with a
+// fused epilogue the launch is data-parallel (one whole tile pair per CTA
+// pair, which tc_pair_data_parallel says is worthwhile and possible).
+bool tc_pair_data_parallel(const TcRuntime &rt, int N);
 // pdl: launch with programmatic stream serialization (the weight stream
 // starts while the previous kernel finishes; activations are read after it).
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,

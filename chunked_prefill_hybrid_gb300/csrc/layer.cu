@@ -222,11 +222,12 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
     const bool pair = ctx->gemm_impl == 2;
     // the pair kernel leaves fp32 partial tiles; a grid-wide pass sums them
     // and applies the fused epilogue
-    ctx->n_launches += (pair ? 2 : 1) * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
+    const int per_slab = (pair && !tc_pair_data_parallel(ctx->fast->rt, N)) ? 2 : 1;
+    ctx->n_launches += per_slab * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
     for (int t0 = 0; t0 < T; t0 += slab) {
         const int Tn = T - t0 < slab ? T - t0 : slab;
         const EpiParams er = epi_rows(ep, t0, Tn);
-        if (!pair) {
+        if (!pair || tc_pair_data_parallel(ctx->fast->rt, N)) {
             cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, er);
             if (e != cudaSuccess)
                 return e;
