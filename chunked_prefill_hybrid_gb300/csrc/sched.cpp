@@ -1,5 +1,6 @@
 // sched.cpp -- the host decode-maximal scheduler behind include/hb_sched.h.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <deque>
 #include <map>
@@ -36,7 +37,10 @@ struct hb_sched {
     bool pending = false;
     std::vector<int32_t> spec_dbt;
     hb_sched_stats stats{};
+    double pd_ewma = -1.0;  // P:D of finished requests, exponentially weighted
 };
+
+static constexpr double kPdWeight = 0.125;  // weight of the newest observation
 
 static int blocks_for(const hb_sched_config &c, long long tokens)
 {
@@ -172,6 +176,8 @@ extern "C" int hb_sched_complete(hb_sched *s)
     s->pending = false;
     int finished = 0;
     auto finish = [&](Req &r) {
+        const double pd = (double)r.prompt / (double)r.generated;
+        s->pd_ewma = s->pd_ewma < 0 ? pd : s->pd_ewma + kPdWeight * (pd - s->pd_ewma);
         r.phase = DONE;
         for (int32_t b : r.blocks)
             s->free_blocks.insert(b);
@@ -270,3 +276,38 @@ extern "C" long long hb_sched_max_batch(long long mem_total, long long mem_param
 }
 
 extern "C" void hb_sched_free(hb_sched *s) { delete s; }
+
+extern "C" double hb_perfect_pd_ratio(int chunk_size, int batch_size)
+{
+    if (chunk_size < 1 || batch_size < 2)
+        return -1.0;
+    return (double)chunk_size / (double)(batch_size - 1);
+}
+
+extern "C" long long hb_piggyback_capacity(long long prompt_len, long long decode_len, int chunk_size, int batch_size)
+{
+    if (prompt_len < 1 || decode_len < 0 || chunk_size < 1 || batch_size < 1)
+        return -1;
+    const long long chunks = (prompt_len + chunk_size - 1) / chunk_size;
+    const long long cap = chunks * (long long)(batch_size - 1);
+    return decode_len < cap ? decode_len : cap;
+}
+
+extern "C" int hb_advise_chunk(double pd_ratio, int batch_size, int tile, int c_min, int c_max)
+{
+    if (!(pd_ratio > 0) || batch_size < 2 || c_min < 1 || c_max < c_min || tile < 0)
+        return -1;
+    const double want = pd_ratio * (double)(batch_size - 1);
+    long long c0 = (long long)std::llround(want);
+    if (c0 < c_min)
+        c0 = c_min;
+    if (c0 > c_max)
+        c0 = c_max;
+    if (tile == 0)
+        return (int)c0;
+    const long long rows = c0 + batch_size - 1;
+    const long long c = rows / tile * tile - (batch_size - 1);
+    return (int)(c >= c_min ? c : c0);
+}
+
+extern "C" double hb_sched_pd_estimate(hb_sched *s) { return s ? s->pd_ewma : -1.0; }

@@ -54,7 +54,11 @@ def _lib():
                 ("hb_sched_fill_spec", [vp, P(native.BatchSpec)], ci),
                 ("hb_sched_get_stats", [vp, P(_Stats)], ci),
                 ("hb_sched_max_batch", [ctypes.c_longlong] * 4, ctypes.c_longlong),
-                ("hb_sched_free", [vp], None)):
+                ("hb_sched_free", [vp], None),
+                ("hb_perfect_pd_ratio", [ci, ci], ctypes.c_double),
+                ("hb_piggyback_capacity", [ctypes.c_longlong, ctypes.c_longlong, ci, ci], ctypes.c_longlong),
+                ("hb_advise_chunk", [ctypes.c_double, ci, ci, ci, ci], ci),
+                ("hb_sched_pd_estimate", [vp], ctypes.c_double)):
             f = getattr(L, name)
             f.argtypes = args
             f.restype = res
@@ -64,6 +68,18 @@ def _lib():
 
 def max_batch(mem_total: int, mem_params: int, max_len: int, kv_bytes_per_token: int) -> int:
     return int(_lib().hb_sched_max_batch(mem_total, mem_params, max_len, kv_bytes_per_token))
+
+
+def perfect_pd_ratio(chunk_size: int, batch_size: int) -> float:
+    return float(_lib().hb_perfect_pd_ratio(chunk_size, batch_size))
+
+
+def piggyback_capacity(prompt_len: int, decode_len: int, chunk_size: int, batch_size: int) -> int:
+    return int(_lib().hb_piggyback_capacity(prompt_len, decode_len, chunk_size, batch_size))
+
+
+def advise_chunk(pd_ratio: float, batch_size: int, tile: int = 0, c_min: int = 1, c_max: int = 1 << 30) -> int:
+    return int(_lib().hb_advise_chunk(pd_ratio, batch_size, tile, c_min, c_max))
 
 
 class Scheduler:
@@ -113,6 +129,9 @@ class Scheduler:
         if rc:
             raise native.HbError(rc, "hb_sched_fill_spec")
         return self._spec
+
+    def pd_estimate(self) -> float:
+        return float(_lib().hb_sched_pd_estimate(self.h))
 
     def stats(self) -> dict:
         st = _Stats()

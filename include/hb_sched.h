@@ -114,6 +114,29 @@ long long hb_sched_max_batch(long long mem_total, long long mem_params, long lon
 
 void hb_sched_free(hb_sched *s);
 
+/* ---- chunk-size selection ("SARATHI ..." summary, section "The chunk size",
+ * "The piggybacking condition" and "A two-step chunk selection procedure").
+ * All host-only; no scheduler state unless stated. */
+
+/* P:D ratio at which every decode of a request is piggybacked:
+ * C / (B - 1).  Returns -1 for C < 1 or B < 2. */
+double hb_perfect_pd_ratio(int chunk_size, int batch_size);
+
+/* Decode tokens of a request (prompt P, D decode tokens) that can ride on its
+ * prefill chunks: min(D, ceil(P / C) * (B - 1)).  -1 for bad arguments. */
+long long hb_piggyback_capacity(long long prompt_len, long long decode_len, int chunk_size, int batch_size);
+
+/* Two-step chunk size: (1) C0 = round(pd_ratio * (B - 1)) clamped to
+ * [c_min, c_max]; (2) if tile > 0, the largest C <= C0 with C + (B - 1) a
+ * multiple of tile, provided C >= c_min (else C0).  Returns -1 for bad
+ * arguments (pd_ratio <= 0, B < 2, c_min < 1, c_max < c_min, tile < 0). */
+int hb_advise_chunk(double pd_ratio, int batch_size, int tile, int c_min, int c_max);
+
+/* Online estimate of the workload's P:D ratio: an exponentially weighted
+ * mean (weight 1/8 per observation) of prompt_len / tokens produced over the
+ * requests the scheduler has finished; -1 before the first one. */
+double hb_sched_pd_estimate(hb_sched *s);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

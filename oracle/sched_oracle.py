@@ -39,6 +39,7 @@ class SchedOracle:
         self.waiting = []      # FCFS
         self.running = []      # admission order
         self.last = None
+        self.pd_ewma = None
 
     def blocks_needed(self, prompt, max_new):
         return math.ceil((prompt + max_new) / self.bs)
@@ -117,6 +118,10 @@ class SchedOracle:
 
     def _finish(self, rid):
         r = self.req[rid]
+        # online P:D estimate: exponentially weighted, weight 1/8 for the newest
+        # finished request (the pages name an EWMA and leave its weight open)
+        pd = r["prompt"] / r["generated"]
+        self.pd_ewma = pd if self.pd_ewma is None else self.pd_ewma + (pd - self.pd_ewma) / 8
         r["phase"] = "done"
         self.free = sorted(self.free + r["blocks"])
         r["blocks"] = []
@@ -126,3 +131,29 @@ class SchedOracle:
 def max_batch(mem_total, mem_params, max_len, kv_bytes_per_token):
     """B = floor((M_G - M_S) / (L * m_kv)) (SARATHI summary, "The Memory Constraint")."""
     return (mem_total - mem_params) // (max_len * kv_bytes_per_token)
+
+
+def perfect_pd_ratio(C, B):
+    """P/D at which every decode rides on a prefill chunk: P/D = C / (B - 1)
+    (SARATHI summary, "The piggybacking condition")."""
+    return C / (B - 1)
+
+
+def piggyback_capacity(P, D, C, B):
+    """Decode tokens of one request that fit on its ceil(P/C) chunks of B - 1
+    decode slots each: min(D, (P/C)(B - 1)) with P/C rounded up."""
+    return min(D, math.ceil(P / C) * (B - 1))
+
+
+def advise_chunk(pd, B, tile=0, c_min=1, c_max=1 << 30):
+    """The pages' two-step choice ("A two-step chunk selection procedure"):
+    C ~ (P/D)(B - 1), then round down so that C + (B - 1) is a multiple of the
+    tile (256 - (B - 1) for a chunk of 256 and tile 128)."""
+    x = pd * (B - 1)
+    r = math.floor(x) + (1 if x - math.floor(x) >= 0.5 else 0)  # nearest, halves up
+    c0 = min(max(r, c_min), c_max)
+    if tile == 0:
+        return c0
+    rows = c0 + B - 1
+    c = (rows // tile) * tile - (B - 1)
+    return c if c >= c_min else c0

@@ -223,3 +223,72 @@ def test_fill_spec_is_a_valid_forward_batch():
             seen_decode = True
         s.complete()
     assert seen_decode
+
+
+def test_chunk_advisor_worked_examples():
+    for l in _lines("chunk_advisor.txt"):
+        if l[0] == "perfect":
+            C, B, printed = int(l[1]), int(l[2]), float(l[3])
+            for f in (sched.perfect_pd_ratio, sched_oracle.perfect_pd_ratio):
+                assert abs(f(C, B) - printed) <= 0.1 * printed  # the pages print it rounded
+            assert abs(sched.perfect_pd_ratio(C, B) - C / (B - 1)) < 1e-12
+        elif l[0] == "advise":
+            pd, B, tile, want = float(l[1]), int(l[2]), int(l[3]), int(l[4])
+            assert sched.advise_chunk(pd, B, tile) == want
+            assert sched_oracle.advise_chunk(pd, B, tile) == want
+
+
+def test_chunk_advisor_matches_oracle_and_invariants():
+    rng = random.Random(3)
+    for _ in range(3000):
+        B = rng.randint(2, 200)
+        pd = rng.choice([rng.uniform(0.1, 300), rng.randint(1, 50) / 2])
+        tile = rng.choice([0, 16, 64, 128, 256])
+        c_min = rng.randint(1, 64)
+        c_max = c_min + rng.randint(0, 4096)
+        a = sched.advise_chunk(pd, B, tile, c_min, c_max)
+        assert a == sched_oracle.advise_chunk(pd, B, tile, c_min, c_max), (pd, B, tile, c_min, c_max)
+        assert c_min <= a <= c_max
+        if tile and a != sched_oracle.advise_chunk(pd, B, 0, c_min, c_max):
+            assert (a + B - 1) % tile == 0  # aligned whenever alignment changed it
+    # at the perfect ratio the untiled advice is the chunk itself
+    for C in (64, 128, 239, 256, 512):
+        for B in (2, 5, 18, 64):
+            assert sched.advise_chunk(sched.perfect_pd_ratio(C, B), B) == C
+    assert sched.advise_chunk(0, 18) == -1 and sched.advise_chunk(10, 1) == -1
+
+
+def test_piggyback_capacity_condition():
+    rng = random.Random(4)
+    for _ in range(2000):
+        P, D, C, B = rng.randint(1, 4096), rng.randint(0, 4096), rng.randint(1, 1024), rng.randint(1, 64)
+        cap = sched.piggyback_capacity(P, D, C, B)
+        assert cap == sched_oracle.piggyback_capacity(P, D, C, B)
+        # every decode rides a chunk exactly when ceil(P/C)(B-1) >= D
+        assert (cap == D) == (-(-P // C) * (B - 1) >= D)
+    # the pages' steady state: a 1024-token prompt at C = 256 carries 4 x 17 decodes
+    assert sched.piggyback_capacity(1024, 68, 256, 18) == 68
+    assert sched.piggyback_capacity(1024, 69, 256, 18) == 68
+
+
+@pytest.mark.parametrize("impl", ["lib", "oracle"])
+def test_pd_estimate_tracks_finished_requests(impl):
+    s = (sched.Scheduler if impl == "lib" else sched_oracle.SchedOracle)(chunk_size=64)
+    est = (lambda: s.pd_estimate()) if impl == "lib" else (lambda: -1.0 if s.pd_ewma is None else s.pd_ewma)
+    assert est() == -1.0
+    s.add(1, 100, 4)  # P:D = 25
+    while True:
+        b = s.next()
+        rows = b.n_rows if impl == "lib" else b[2]
+        if rows == 0:
+            break
+        s.complete()
+    assert abs(est() - 25.0) < 1e-12
+    s.add(2, 60, 2)  # P:D = 30: 25 + (30 - 25) / 8
+    while True:
+        b = s.next()
+        rows = b.n_rows if impl == "lib" else b[2]
+        if rows == 0:
+            break
+        s.complete()
+    assert abs(est() - 25.625) < 1e-12
