@@ -282,6 +282,42 @@ TRAFFIC_PROFILES = {
 }
 
 
+TILE_CURVE_CHUNKS = list(range(200, 321)) + [64, 128, 384, 494, 512, 1024]
+
+
+def tile_curve(args, torch, native, workloads, synth, world, rank):
+    """Layer time against the chunk size C (LLaMA-13B layer, chunk at offset
+    768, 18 decodes at ctx 1024): the GB300 form of the pages' tile-quantization
+    curve (SARATHI summary, "The tile quantization effect", Figure 7: 256 vs 257).  The
+    step in time every `quantum` rows of T = C + 18 is the tile a chunk size
+    should be aligned to."""
+    cmax = max(TILE_CURVE_CHUNKS)
+    w = workloads.make("llama13b-tile-curve", synth.LLAMA_13B, 2 + rank, 768, cmax, [1024] * 18)
+    ctx = native.Context(workloads.config(w))
+    x = workloads.upload(w, ctx, poison=None)
+    steps = max(10, min(args.steps, 50))
+    points = []
+    for C in sorted(TILE_CURVE_CHUNKS):
+        b = synth.HybridBatch(w.batch.chunk, C, w.batch.decodes)
+        spec = native.Spec(b)
+        xc = torch.cat([x[:C], x[cmax:]]).contiguous()
+        yc = torch.empty_like(xc)
+        fn = lambda: ctx.forward(spec, xc, yc)
+        for _ in range(args.warmup):
+            fn()
+        ctx.sync()
+        ms = max_over_ranks(world, time_steps(torch, ctx, fn, steps, world)) / steps
+        points.append({"chunk": C, "T": C + 18, "ms": round(ms, 5), "tok_s": round((C + 18) / ms * 1e3)})
+    ctx.free()
+    # rows at which the time steps up by more than 1.5 % over the previous chunk size
+    steps_at = [p["T"] for a, p in zip(points, points[1:])
+                if p["chunk"] == a["chunk"] + 1 and p["ms"] > a["ms"] * 1.015]
+    if rank == 0:
+        print(json.dumps({"tile_curve": WORKLOAD.replace("c256", "cX"), "steps_timed": steps,
+                          "step_up_at_T": steps_at, "points": points}), flush=True)
+    return 0
+
+
 def sources_sha256(names):
     import hashlib
     h = hashlib.sha256()
@@ -356,6 +392,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tile-curve", action="store_true",
+                    help="time the LLaMA-13B hybrid layer against the chunk size (18 decodes at ctx 1024) and print "
+                         "one JSON line with the curve instead of the benchmark line")
     ap.add_argument("--ncu-case", action="store_true",
                     help="run only the warm-up and --steps hybrid steps, untimed (the case ncu captures)")
     args = ap.parse_args()
@@ -370,6 +409,9 @@ def main():
     import __graft_entry__
     __graft_entry__.build_library()
     from chunked_prefill_hybrid_gb300 import native, workloads, synth
+
+    if args.tile_curve:
+        return tile_curve(args, torch, native, workloads, synth, world, rank)
 
     w = workloads.llama13b_hybrid(seed=2 + rank)
     dims = w.dims
