@@ -44,11 +44,11 @@ struct FastPath {
     std::vector<CUtensorMap> kv_maps;  // [layer][K, V] pool maps of the tcgen05 chunk attention
 };
 
-static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + 1; }
+static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + HB_MAX_CHUNKS; }
 static size_t max_splits_per_seq(const hb_model_config &c) { return (size_t)(c.max_pos + 1) / ATTN_SPLIT + 1; }
 static size_t max_items(const hb_model_config &c)
 {
-    return ((size_t)c.max_tokens + 63) / 64 + max_seqs(c) * max_splits_per_seq(c);
+    return ((size_t)c.max_tokens + 63) / 64 + HB_MAX_CHUNKS + max_seqs(c) * max_splits_per_seq(c);
 }
 
 size_t kMetaExtraWords(const hb_model_config &c) { return 2 * max_items(c) + max_seqs(c); }

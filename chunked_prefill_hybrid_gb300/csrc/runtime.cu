@@ -95,7 +95,32 @@ int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::s
         return fail(err, HB_EINVAL, "n_decodes < 0");
     if (s->n_decodes > c.max_decodes)
         return fail(err, HB_ERANGE, "n_decodes %d > max_decodes %d", s->n_decodes, c.max_decodes);
-    const int clen = has_chunk ? s->chunk_len : 0;
+    const int n_more = s->n_more_chunks;
+    if (n_more < 0)
+        return fail(err, HB_EINVAL, "n_more_chunks < 0");
+    if (n_more > 0) {
+        if (!has_chunk)
+            return fail(err, HB_EINVAL, "further chunks need a first chunk (chunk_req_id >= 0)");
+        if (n_more > HB_MAX_CHUNKS - 1)
+            return fail(err, HB_ERANGE, "%d chunks > HB_MAX_CHUNKS %d", n_more + 1, HB_MAX_CHUNKS);
+        if (!s->more_chunk_req_ids || !s->more_chunk_offsets || !s->more_chunk_lens || !s->more_chunk_block_tables)
+            return fail(err, HB_EINVAL, "further-chunk arrays are NULL");
+        if (s->more_chunk_bt_stride <= 0 || s->more_chunk_bt_stride > c.max_blocks_per_seq)
+            return fail(err, HB_ERANGE, "more_chunk_bt_stride %d outside 1..max_blocks_per_seq",
+                        s->more_chunk_bt_stride);
+        for (int i = 0; i < n_more; ++i) {
+            if (s->more_chunk_lens[i] <= 0)
+                return fail(err, HB_EINVAL, "further chunk %d: length must be > 0", i);
+            if (s->more_chunk_offsets[i] < 0)
+                return fail(err, HB_EINVAL, "further chunk %d: offset must be >= 0", i);
+        }
+    }
+    long long chunk_rows = has_chunk ? s->chunk_len : 0;
+    for (int i = 0; i < n_more; ++i)
+        chunk_rows += s->more_chunk_lens[i];
+    if (chunk_rows > c.max_tokens)
+        return fail(err, HB_ERANGE, "chunks hold %lld rows > max_tokens %d", chunk_rows, c.max_tokens);
+    const int clen = (int)chunk_rows;
     const long long T = (long long)clen + s->n_decodes;
     if (T <= 0)
         return fail(err, HB_EINVAL, "empty batch (no chunk and no decodes)");
@@ -115,13 +140,18 @@ int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::s
                 return fail(err, HB_EINVAL, "decode request ids must be >= 0");
         if (has_chunk)
             ids.push_back(s->chunk_req_id);
+        for (int i = 0; i < n_more; ++i) {
+            if (s->more_chunk_req_ids[i] < 0)
+                return fail(err, HB_EINVAL, "further chunk request ids must be >= 0");
+            ids.push_back(s->more_chunk_req_ids[i]);
+        }
         std::sort(ids.begin(), ids.end());
         if (std::adjacent_find(ids.begin(), ids.end()) != ids.end())
             return fail(err, HB_EINVAL, "duplicate request id in the batch (decode ids and the chunk id must differ)");
     }
     p.T = (int)T;
     p.chunk_len = clen;
-    p.n_seq = (has_chunk ? 1 : 0) + s->n_decodes;
+    p.n_seq = (has_chunk ? 1 + n_more : 0) + s->n_decodes;
     p.pos.assign(p.T, 0);
     p.slot.assign(p.T, 0);
     p.row_seq.assign(p.T, 0);
@@ -163,9 +193,18 @@ int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::s
     if (has_chunk) {
         if (s->chunk_n_blocks <= 0)
             return fail(err, HB_ERANGE, "chunk_n_blocks must be > 0");
-        int rc = add_seq(0, clen, s->chunk_offset, s->chunk_block_table, s->chunk_n_blocks, "chunk", 0);
+        int rc = add_seq(0, s->chunk_len, s->chunk_offset, s->chunk_block_table, s->chunk_n_blocks, "chunk", 0);
         if (rc)
             return rc;
+        int q0 = s->chunk_len;
+        for (int i = 0; i < n_more; ++i) {
+            rc = add_seq(q0, s->more_chunk_lens[i], s->more_chunk_offsets[i],
+                         s->more_chunk_block_tables + (size_t)i * s->more_chunk_bt_stride, s->more_chunk_bt_stride,
+                         "further chunk", i);
+            if (rc)
+                return rc;
+            q0 += s->more_chunk_lens[i];
+        }
     }
     for (int j = 0; j < s->n_decodes; ++j) {
         const int ctx = s->decode_ctx_lens[j];
@@ -361,7 +400,7 @@ extern "C" int hb_init(const hb_model_config *cfg, const hb_layer_weights *weigh
         return bail(HB_ECUDA);
 
     // metadata: 3 T + 4 n_seq + block tables + attention work list
-    const size_t max_seq = (size_t)c.max_decodes + 1;
+    const size_t max_seq = (size_t)c.max_decodes + HB_MAX_CHUNKS;
     ctx->meta_cap = 3 * MT + 4 * max_seq + max_seq * c.max_blocks_per_seq + kMetaExtraWords(c);
     if ((rc = ctx_alloc(ctx, (void **)&ctx->d_meta, ctx->meta_cap * sizeof(int))))
         return bail(rc);

@@ -35,7 +35,7 @@ struct hb_sched {
     std::vector<int32_t> c_ids, c_off, c_len, d_ids, d_ctx;
     int n_rows = 0;
     bool pending = false;
-    std::vector<int32_t> spec_dbt;
+    std::vector<int32_t> spec_dbt, spec_mbt, spec_mids;
     hb_sched_stats stats{};
     double pd_ewma = -1.0;  // P:D of finished requests, exponentially weighted
 };
@@ -221,8 +221,8 @@ extern "C" int hb_sched_fill_spec(hb_sched *s, hb_batch_spec *spec)
 {
     if (!s || !spec)
         return HB_EINVAL;
-    if (s->c_ids.size() > 1)
-        return HB_EINVAL;
+    if (s->c_ids.size() > HB_MAX_CHUNKS)
+        return HB_ERANGE;
     std::memset(spec, 0, sizeof *spec);
     spec->chunk_req_id = -1;
     if (!s->c_ids.empty()) {
@@ -234,6 +234,20 @@ extern "C" int hb_sched_fill_spec(hb_sched *s, hb_batch_spec *spec)
         spec->chunk_n_blocks = (int)r.blocks.size();
     }
     const int W = s->cfg.max_blocks_per_seq;
+    const size_t n_more = s->c_ids.empty() ? 0 : s->c_ids.size() - 1;
+    s->spec_mbt.assign(std::max<size_t>(1, n_more) * W, -1);
+    s->spec_mids.assign(std::max<size_t>(1, n_more), 0);
+    for (size_t i = 0; i < n_more; ++i) {
+        const Req &r = s->reqs[s->c_ids[i + 1]];
+        s->spec_mids[i] = r.id;
+        std::copy(r.blocks.begin(), r.blocks.end(), s->spec_mbt.begin() + i * W);
+    }
+    spec->n_more_chunks = (int)n_more;
+    spec->more_chunk_req_ids = s->spec_mids.data();
+    spec->more_chunk_offsets = s->c_off.data() + (n_more ? 1 : 0);
+    spec->more_chunk_lens = s->c_len.data() + (n_more ? 1 : 0);
+    spec->more_chunk_block_tables = s->spec_mbt.data();
+    spec->more_chunk_bt_stride = W;
     s->spec_dbt.assign((size_t)std::max<size_t>(1, s->d_ids.size()) * W, -1);
     for (size_t j = 0; j < s->d_ids.size(); ++j) {
         const Req &r = s->reqs[s->d_ids[j]];

@@ -52,7 +52,12 @@ class BatchSpec(ctypes.Structure):
                 ("chunk_block_table", ctypes.c_void_p), ("chunk_n_blocks", ctypes.c_int),
                 ("n_decodes", ctypes.c_int), ("decode_req_ids", ctypes.c_void_p),
                 ("decode_ctx_lens", ctypes.c_void_p), ("decode_block_tables", ctypes.c_void_p),
-                ("decode_bt_stride", ctypes.c_int)]
+                ("decode_bt_stride", ctypes.c_int), ("n_more_chunks", ctypes.c_int),
+                ("more_chunk_req_ids", ctypes.c_void_p), ("more_chunk_offsets", ctypes.c_void_p),
+                ("more_chunk_lens", ctypes.c_void_p), ("more_chunk_block_tables", ctypes.c_void_p),
+                ("more_chunk_bt_stride", ctypes.c_int)]
+
+HB_MAX_CHUNKS = 16
 
 
 _lib = None
@@ -119,8 +124,18 @@ class Spec:
         self.dbt = synth.padded_decode_tables(batch, stride)
         self.dids = np.array([s.req_id for s in batch.decodes] or [0], np.int32)
         self.dctx = np.array([s.cached for s in batch.decodes] or [0], np.int32)
+        more = list(batch.more_chunks)
+        mstride = max([len(sq.block_table) for sq, _ in more] + [1])
+        self.mbt = np.full((max(len(more), 1), mstride), -1, np.int32)
+        for i, (sq, _) in enumerate(more):
+            self.mbt[i, :len(sq.block_table)] = sq.block_table
+        self.mids = np.array([sq.req_id for sq, _ in more] or [0], np.int32)
+        self.moff = np.array([sq.cached for sq, _ in more] or [0], np.int32)
+        self.mlen = np.array([n for _, n in more] or [0], np.int32)
         self.c = BatchSpec(cid, coff, clen, self.cbt.ctypes.data, len(self.cbt) if batch.chunk is not None else 0,
-                           D, self.dids.ctypes.data, self.dctx.ctypes.data, self.dbt.ctypes.data, stride)
+                           D, self.dids.ctypes.data, self.dctx.ctypes.data, self.dbt.ctypes.data, stride,
+                           len(more), self.mids.ctypes.data, self.moff.ctypes.data, self.mlen.ctypes.data,
+                           self.mbt.ctypes.data, mstride)
 
     @property
     def T(self) -> int:

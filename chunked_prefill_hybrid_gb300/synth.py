@@ -22,7 +22,7 @@ from __future__ import annotations
 
 import dataclasses
 from dataclasses import dataclass, field
-from typing import List, Optional, Sequence
+from typing import List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -147,10 +147,17 @@ class HybridBatch:
     chunk: Optional[Seq]
     chunk_len: int
     decodes: List[Seq] = field(default_factory=list)
+    # further (Seq, length) chunks of other requests, rows after the first
+    # chunk's (Sarathi-Serve batches under a token budget)
+    more_chunks: List[Tuple[Seq, int]] = field(default_factory=list)
+
+    @property
+    def n_chunk_rows(self) -> int:
+        return (self.chunk_len if self.chunk is not None else 0) + sum(n for _, n in self.more_chunks)
 
     @property
     def n_tokens(self) -> int:
-        return (self.chunk_len if self.chunk is not None else 0) + len(self.decodes)
+        return self.n_chunk_rows + len(self.decodes)
 
     @property
     def n_decodes(self) -> int:

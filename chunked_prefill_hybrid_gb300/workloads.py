@@ -41,7 +41,8 @@ class Workload:
 
 def _prefix(seed: int, dims: synth.ModelDims, n_layers: int, batch: synth.HybridBatch):
     out = []
-    seqs = ([batch.chunk] if batch.chunk is not None else []) + list(batch.decodes)
+    seqs = ([batch.chunk] if batch.chunk is not None else []) + [s for s, _ in batch.more_chunks]
+    seqs += list(batch.decodes)
     for layer in range(n_layers):
         for s in seqs:
             if s.cached > 0:

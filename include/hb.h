@@ -102,8 +102,22 @@ typedef struct {
  *                     at position ctx and attends ctx+1 keys
  *   decode_block_tables [n_decodes][decode_bt_stride]; row j covers
  *                     positions 0 .. ctx_j
- * Row order of x_in / x_out: chunk rows 0..chunk_len-1, then decode rows in
- * spec order.  Slot of position p: table[p / 16] * 16 + p % 16. */
+ *   n_more_chunks     further prefill chunks of other requests in the same
+ *                     batch (0 for a SARATHI batch).  Sarathi-Serve's
+ *                     stall-free batching ("Notes on Sarathi-Serve",
+ *                     "Stall Free Batching" and its illustrated example) fills
+ *                     the token budget with several chunks: the partially
+ *                     prefilled request first, then the next in FCFS order.
+ *                     Needs chunk_req_id >= 0; at most HB_MAX_CHUNKS - 1.
+ *   more_chunk_req_ids, more_chunk_offsets, more_chunk_lens [n_more_chunks]:
+ *                     as chunk_req_id / chunk_offset / chunk_len (len > 0;
+ *                     ids distinct from every other id of the batch)
+ *   more_chunk_block_tables [n_more_chunks][more_chunk_bt_stride]; row i
+ *                     covers positions 0 .. offset_i + len_i - 1
+ * Row order of x_in / x_out: chunk rows 0..chunk_len-1, then the rows of each
+ * further chunk in spec order, then decode rows in spec order.  Slot of
+ * position p: table[p / 16] * 16 + p % 16.  A chunk of one row computes what
+ * a decode at ctx = offset computes. */
 typedef struct {
     int chunk_req_id;
     int chunk_offset;
@@ -115,7 +129,16 @@ typedef struct {
     const int32_t *decode_ctx_lens;
     const int32_t *decode_block_tables;
     int decode_bt_stride;
+    int n_more_chunks;
+    const int32_t *more_chunk_req_ids;
+    const int32_t *more_chunk_offsets;
+    const int32_t *more_chunk_lens;
+    const int32_t *more_chunk_block_tables;
+    int more_chunk_bt_stride;
 } hb_batch_spec;
+
+/* Most prefill chunks in one batch (the first plus n_more_chunks). */
+#define HB_MAX_CHUNKS 16
 
 /* Create a context on the current CUDA device.
  * cfg: host.  weights: host array of n_layers entries (device pointers

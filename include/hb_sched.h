@@ -99,9 +99,11 @@ int hb_sched_complete(hb_sched *s);
 /* Block table of an admitted request (scheduler-owned). */
 int hb_sched_block_table(hb_sched *s, int req_id, const int32_t **table, int *n_blocks);
 
-/* Fill an hb_forward spec for the last batch (single-chunk or decode-only
- * batches; HB_EINVAL for more than one chunk).  Block tables point into
- * scheduler-owned storage, decode rows of width max_blocks_per_seq. */
+/* Fill an hb_forward spec for the last batch: its first chunk in the chunk_*
+ * fields, further chunks (max_chunks_per_batch > 1) in the more_chunk_*
+ * fields, decodes after them (HB_ERANGE beyond HB_MAX_CHUNKS chunks).  Block
+ * tables point into scheduler-owned storage, rows of width
+ * max_blocks_per_seq, valid until the next hb_sched_* call. */
 int hb_sched_fill_spec(hb_sched *s, hb_batch_spec *spec);
 
 int hb_sched_get_stats(hb_sched *s, hb_sched_stats *out);

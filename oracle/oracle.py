@@ -218,6 +218,9 @@ def layer_forward(dims, weights: dict, batch, x_in: np.ndarray, pool: Pool, mirr
     boolean mask of rows to compute.  Returns y [T][hidden] (rows not
     selected are NaN) and, if aux, a dict of intermediates.
     """
+    more = list(getattr(batch, "more_chunks", None) or [])
+    if more:
+        return _forward_split(dims, weights, batch, more, x_in, pool, mirror, rows, aux, mutate)
     L = load(mutate)
     T = batch.n_tokens
     H = dims.hidden
@@ -257,6 +260,42 @@ def layer_forward(dims, weights: dict, batch, x_in: np.ndarray, pool: Pool, mirr
     if rc:
         raise OracleError(f"oracle_layer_forward returned {rc}")
     return (y, bufs) if aux else y
+
+
+class _Part:
+    """A batch of one chunk (or none) and some decodes."""
+
+    def __init__(self, chunk, chunk_len, decodes):
+        self.chunk, self.chunk_len, self.decodes = chunk, chunk_len, decodes
+        self.n_tokens = (chunk_len if chunk is not None else 0) + len(decodes)
+
+
+def _forward_split(dims, weights, batch, more, x_in, pool, mirror, rows, aux, mutate):
+    """A batch with several chunks: rows of different requests never meet
+    (each attends only its own request's keys), so the first chunk with the
+    decodes, and each further chunk on its own, give the batch's rows.  Row
+    order: first chunk, further chunks in order, decodes."""
+    if aux:
+        raise OracleError("aux intermediates are only kept for single-chunk batches")
+    T, H = x_in.shape
+    c0 = batch.chunk_len if batch.chunk is not None else 0
+    starts, at = [], c0
+    for _, n in more:
+        starts.append(at)
+        at += n
+    dec = np.arange(at, T)
+    y = np.full((T, H), np.nan, np.float64)
+    sel = None if rows is None else np.asarray(rows).astype(bool)
+    first = np.concatenate([np.arange(c0), dec]).astype(np.int64)
+    parts = [(first, _Part(batch.chunk, c0, list(batch.decodes)))]
+    for (seq, n), q0 in zip(more, starts):
+        parts.append((np.arange(q0, q0 + n), _Part(seq, n, [])))
+    for idx, part in parts:
+        if part.n_tokens == 0:
+            continue
+        y[idx] = layer_forward(dims, weights, part, np.ascontiguousarray(x_in[idx]), pool, mirror=mirror,
+                               rows=None if sel is None else sel[idx], mutate=mutate)
+    return y
 
 
 def set_threads(n: int, mutate: int = 0):

@@ -300,6 +300,29 @@ def pin_layer_textbook_hybrid(mutate=0):
     assert np.allclose(y, ref, rtol=1e-10, atol=1e-10), np.abs(y - ref).max()
 
 
+def pin_layer_textbook_two_chunks(mutate=0):
+    """A Sarathi-Serve batch: the leftover chunk of a partially prefilled
+    request (16 at offset 24 of 40), the first 10 tokens of a new request,
+    and two decodes ("Notes on Sarathi-Serve", "Stall Free Batching",
+    illustrated example), against the textbook layer per request."""
+    dims = PIN_DIMS
+    w, full, tab, pool, batch, x = _hybrid_case(dims, 27, mutate)
+    H = dims.hidden
+    full["D"] = _seq_rows(27, (5,), 18, H)
+    tD = np.arange(12, 14, dtype=np.int32)
+    big = orc.Pool(14, dims.n_kv_heads, dims.head_dim)
+    big.k[:pool.k.shape[0]] = pool.k
+    big.v[:pool.v.shape[0]] = pool.v
+    two = synth.HybridBatch(batch.chunk, batch.chunk_len, batch.decodes, [(synth.Seq(3, 0, tD), 10)])
+    xx = np.concatenate([x[:16], full["D"][:10], x[16:]])
+    y = orc.layer_forward(dims, w, two, xx, big, mirror=False, mutate=mutate)
+    ref = np.concatenate([textbook.layer_full_sequence(dims, w, full["A"])[0][24:40],
+                          textbook.layer_full_sequence(dims, w, full["D"])[0][0:10],
+                          textbook.layer_full_sequence(dims, w, full["B"])[0][5:6],
+                          textbook.layer_full_sequence(dims, w, full["C"])[0][17:18]])
+    assert np.allclose(y, ref, rtol=1e-10, atol=1e-10), np.abs(y - ref).max()
+
+
 def pin_layer_textbook_gqa(mutate=0):
     dims = GQA_DIMS
     w, full, tab, pool, batch, x = _hybrid_case(dims, 23, mutate, gamma="uniform")

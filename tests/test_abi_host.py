@@ -130,3 +130,67 @@ def test_decode_only_and_prefill_only_plans(L):
     pos, slot = native.plan(_cfg(), native.Spec(b))
     assert list(pos) == list(range(100))
     assert len(set(slot.tolist())) == 100
+
+
+def _multi(seed=10, n_more=2, nb=96):
+    """First chunk 8 @ 10, further chunks (5 @ 0, 12 @ 30, ...) and decodes at 5 and 9."""
+    more_shapes = [(0, 5), (30, 12), (3, 1)][:n_more] + [(0, 2)] * max(0, n_more - 3)
+    lengths = [18, 6, 10] + [o + n for o, n in more_shapes]
+    tabs = synth.allocate_tables(seed, (1,), lengths, nb)
+    b = synth.HybridBatch(synth.Seq(0, 10, tabs[0]), 8, [synth.Seq(1, 5, tabs[1]), synth.Seq(2, 9, tabs[2])],
+                          [(synth.Seq(10 + i, o, tabs[3 + i]), n) for i, (o, n) in enumerate(more_shapes)])
+    return b
+
+
+def test_plan_several_chunks_rows_and_slots(L):
+    b = _multi()
+    pos, slot = native.plan(_cfg(num_blocks=96), native.Spec(b))
+    assert b.n_tokens == 8 + 5 + 12 + 2
+    exp = list(range(10, 18)) + list(range(0, 5)) + list(range(30, 42)) + [5, 9]
+    assert list(pos) == exp
+    seqs = [b.chunk] * 8 + [b.more_chunks[0][0]] * 5 + [b.more_chunks[1][0]] * 12 + b.decodes
+    for r, (p, s) in enumerate(zip(pos, slot)):
+        assert s == orc.slot(seqs[r].block_table, int(p), 96)
+
+
+def test_plan_several_chunks_rejects(L):
+    cfg = _cfg(num_blocks=96)
+    # HB_MAX_CHUNKS chunks are fine, one more is not
+    tabs = synth.allocate_tables(11, (1,), [2] * 17, 96)
+    b = synth.HybridBatch(synth.Seq(0, 0, tabs[0]), 2, [],
+                          [(synth.Seq(1 + i, 0, tabs[1 + i]), 2) for i in range(native.HB_MAX_CHUNKS - 1)])
+    assert len(native.plan(cfg, native.Spec(b))[0]) == 2 * native.HB_MAX_CHUNKS
+    b.more_chunks.append((synth.Seq(99, 0, tabs[16]), 2))
+    with pytest.raises(native.HbError) as e:
+        native.plan(cfg, native.Spec(b))
+    assert e.value.code == native.HB_ERANGE
+    # further chunks without a first chunk
+    b = _multi()
+    s = native.Spec(b)
+    s.c.chunk_req_id, s.c.chunk_len = -1, 0
+    with pytest.raises(native.HbError) as e:
+        native.plan(cfg, s)
+    assert e.value.code == native.HB_EINVAL
+    # a further chunk of length 0, a duplicate id, overlapping tables, a short table
+    for how, code in (("len0", native.HB_EINVAL), ("dup", native.HB_EINVAL), ("overlap", native.HB_EINVAL),
+                      ("short", native.HB_ERANGE), ("neg", native.HB_EINVAL)):
+        b = _multi()
+        seq, n = b.more_chunks[1]
+        if how == "len0":
+            b.more_chunks[1] = (seq, 0)
+        elif how == "dup":
+            seq.req_id = b.decodes[0].req_id
+        elif how == "overlap":
+            seq.block_table = b.chunk.block_table.copy()
+            seq.cached, b.more_chunks[1] = 10, (seq, 8)
+        elif how == "short":
+            b.more_chunks[1] = (seq, n + 16)
+        else:
+            seq.cached = -1
+        with pytest.raises(native.HbError) as e:
+            native.plan(cfg, native.Spec(b))
+        assert e.value.code == code, how
+    # rows of all chunks count against max_tokens
+    with pytest.raises(native.HbError) as e:
+        native.plan(_cfg(num_blocks=96, max_tokens=26), native.Spec(_multi()))
+    assert e.value.code == native.HB_ERANGE

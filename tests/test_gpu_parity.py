@@ -40,10 +40,13 @@ def run_gpu(w, ctx=None, max_tokens=None, max_decodes=None, poison=True, kernels
 def check_kv(ctx, w, pools, layer=0):
     """Written slots hold the oracle's K/V; the rest of the pool is poison."""
     dims = w.dims
-    seqs = ([w.batch.chunk] if w.batch.chunk is not None else []) + list(w.batch.decodes)
+    rows = ([(w.batch.chunk, w.batch.chunk_len)] if w.batch.chunk is not None else []) + list(w.batch.more_chunks)
+    rows += [(s, 1) for s in w.batch.decodes]
+    seqs = [s for s, _ in rows]
+    written = {id(s): s.cached + n for s, n in rows}
     nkv, d = dims.n_kv_heads, dims.head_dim
     for s in seqs:
-        n = s.cached + (w.batch.chunk_len if s is w.batch.chunk else 1)
+        n = written[id(s)]
         k = torch.empty((n, nkv, d), dtype=torch.int16, device="cuda")
         v = torch.empty_like(k)
         ctx.read_kv(layer, s.block_table, 0, k, v)
@@ -62,7 +65,7 @@ def check_kv(ctx, w, pools, layer=0):
         kb, vb = _bits(k), _bits(v)
         used = set()
         for s in seqs:
-            n = s.cached + (w.batch.chunk_len if s is w.batch.chunk else 1)
+            n = written[id(s)]
             for p in range(n):
                 used.add(int(s.block_table[p // 16]) * 16 + p % 16)
         unused = np.array(sorted(set(range(w.num_blocks * 16)) - used), np.int64)
@@ -192,6 +195,36 @@ def test_piggybacked_decode_matches_alone():
 @pytest.mark.parametrize("T,N,K", [(1, 256, 256), (18, 768, 256), (68, 1376, 688), (274, 512, 5120),
                                    (300, 384, 1024), (513, 256, 512), (16, 130, 64), (1100, 640, 192),
                                    (1500, 384, 128), (2048, 256, 64)])
+def _several_chunks(dims, seed):
+    """A Sarathi-Serve batch: the leftover 40 rows of a prompt at offset 24, a new prompt's first 70 rows
+    (two 64-row tiles and a tail), a one-row chunk at offset 9, 17 rows at offset 100, and decodes at
+    contexts 5, 300 and 77 ("Notes on Sarathi-Serve", "Stall Free Batching")."""
+    shapes = [(24, 40), (0, 70), (9, 1), (100, 17)]
+    ctxs = [5, 300, 77]
+    lengths = [o + n for o, n in shapes] + [c + 1 for c in ctxs]
+    nb = sum(synth.blocks_needed(n) for n in lengths) + 6
+    w = _tiny(seed, 24, 40, ctxs, dims=dims)
+    tabs = synth.allocate_tables(seed, (3,), lengths, nb)
+    b = synth.HybridBatch(synth.Seq(0, 24, tabs[0]), 40, [synth.Seq(10 + j, c, tabs[4 + j]) for j, c in enumerate(ctxs)],
+                          [(synth.Seq(1 + i, o, tabs[1 + i]), n) for i, (o, n) in enumerate(shapes[1:])])
+    w.batch, w.num_blocks, w.max_pos = b, nb, nb * 16
+    w.x = synth.token_rows(seed, (8, 1), b.n_tokens, dims.hidden)
+    w.prefix = workloads._prefix(seed, dims, 1, b)
+    return w
+
+
+@pytest.mark.parametrize("kern", sorted(KERNELS))
+@pytest.mark.parametrize("dims", [synth.TINY, D128, GQA], ids=["tiny", "d128", "gqa"])
+def test_several_chunks_match_oracle(dims, kern):
+    w = _several_chunks(dims, 45)
+    ctx, y = run_gpu(w, kernels=KERNELS[kern])
+    ref, pools = oracle_run(w)
+    ok, st = compare(y, ref)
+    assert ok, (kern, st)
+    check_kv(ctx, w, pools)
+    ctx.free()
+
+
 def test_gemm_kernel_against_fp64(impl, T, N, K):
     w = workloads.tiny(seed=1)
     ctx = native.Context(workloads.config(w))

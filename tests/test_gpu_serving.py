@@ -19,14 +19,15 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-@pytest.mark.parametrize("mode", ["sarathi", "budget"])
+@pytest.mark.parametrize("mode", ["sarathi", "budget", "multi"])
 def test_serving_loop_matches_oracle(mode):
     seed = 41
     dims = synth.TINY.with_layers(2)
     H = dims.hidden
     num_blocks, mbs = 96, 32
     kw = dict(chunk_size=32, num_blocks=num_blocks, max_blocks_per_seq=mbs)
-    kw.update(dict(max_decodes=6) if mode == "sarathi" else dict(token_budget=40))
+    kw.update({"sarathi": dict(max_decodes=6), "budget": dict(token_budget=40),
+               "multi": dict(token_budget=48, max_chunks_per_batch=3)}[mode])
     lib, ref = sched.Scheduler(**kw), sched_oracle.SchedOracle(**kw)
     rng = np.random.default_rng(seed)
     reqs = [(i, int(rng.integers(10, 90)), int(rng.integers(2, 9))) for i in range(7)]
@@ -44,7 +45,7 @@ def test_serving_loop_matches_oracle(mode):
     ctx.sync()
     pools = [orc.Pool(num_blocks, dims.n_kv_heads, dims.head_dim) for _ in range(2)]
 
-    steps = 0
+    steps, most_chunks = 0, 0
     while True:
         b = lib.next()
         chunks, decodes, rows = ref.next()
@@ -64,12 +65,10 @@ def test_serving_loop_matches_oracle(mode):
         ctx.sync()
         gpu = f64(yd.cpu().numpy().view(np.uint16))
         # the oracle replays the same batch through both layers
-        chunk = None
-        if chunks:
-            rid, off, ln = chunks[0]
-            chunk = synth.Seq(rid, off, np.array(ref.req[rid]["blocks"], np.int32))
+        seqs = [(synth.Seq(rid, off, np.array(ref.req[rid]["blocks"], np.int32)), ln) for rid, off, ln in chunks]
         dec = [synth.Seq(rid, c, np.array(ref.req[rid]["blocks"], np.int32)) for rid, c in decodes]
-        hb_ = synth.HybridBatch(chunk, chunks[0][2] if chunks else 0, dec)
+        hb_ = synth.HybridBatch(seqs[0][0] if seqs else None, seqs[0][1] if seqs else 0, dec, seqs[1:])
+        most_chunks = max(most_chunks, len(chunks))
         y = f64(x)
         for l in range(2):
             y = orc.layer_forward(dims, weights[l], hb_, y, pools[l], mirror=True)
@@ -79,5 +78,6 @@ def test_serving_loop_matches_oracle(mode):
         ref.complete()
         steps += 1
     assert steps > 10
+    assert most_chunks == 1 if mode != "multi" else most_chunks > 1
     assert lib.stats()["finished"] == len(reqs)
     ctx.free()

@@ -201,28 +201,35 @@ def test_decodes_never_stall_under_budget():
     assert lib.stats()["finished"] == 12
 
 
-def test_fill_spec_is_a_valid_forward_batch():
-    s = sched.Scheduler(chunk_size=24, token_budget=40, num_blocks=200, max_blocks_per_seq=32)
+@pytest.mark.parametrize("max_chunks", [1, 4])
+def test_fill_spec_is_a_valid_forward_batch(max_chunks):
+    s = sched.Scheduler(chunk_size=24, token_budget=40, num_blocks=200, max_blocks_per_seq=32,
+                        max_chunks_per_batch=max_chunks)
     for i in range(5):
         s.add(i, 30 + 7 * i, 6)
+    s.add(9, 3, 2)
     cfg = native.model_config(synth.TINY, num_blocks=200, max_tokens=40, max_decodes=40, max_pos=512)
-    seen_decode = False
-    for _ in range(30):
+    seen_decode, most_chunks = False, 0
+    for _ in range(40):
         b = s.next()
         if b.n_rows == 0:
             break
         spec = s.fill_spec()
+        assert spec.n_more_chunks == max(0, len(b.chunks) - 1)
         holder = type("H", (), {"c": spec, "T": b.n_rows})
         pos, slot = native.plan(cfg, holder)
         assert len(pos) == b.n_rows
-        if b.chunks:
-            rid, off, ln = b.chunks[0]
-            assert list(pos[:ln]) == list(range(off, off + ln))
+        at = 0
+        for rid, off, ln in b.chunks:   # chunk rows in the scheduler's order, then the decodes
+            assert list(pos[at:at + ln]) == list(range(off, off + ln))
+            at += ln
+        most_chunks = max(most_chunks, len(b.chunks))
         for j, (rid, ctx) in enumerate(b.decodes):
-            assert pos[len(pos) - len(b.decodes) + j] == ctx
+            assert pos[at + j] == ctx
             seen_decode = True
         s.complete()
     assert seen_decode
+    assert (most_chunks == 1) if max_chunks == 1 else (2 <= most_chunks <= max_chunks)
 
 
 def test_chunk_advisor_worked_examples():
