@@ -318,6 +318,56 @@ def tile_curve(args, torch, native, workloads, synth, world, rank):
     return 0
 
 
+def serve_bench(args, torch, native, workloads, synth, world, rank):
+    """LLaMA-33B, 60 layers, serving a closed set of requests present at t = 0:
+    prompts uniform in [512, 2048], max_new = max(1, round(P / r)) for each P:D
+    ratio r; decode-maximal batching with chunks of 256 under a 512-token budget
+    (Sarathi-Serve) against the request-level baseline (prefill-only and
+    decode-only batches) on the same kernels.  KV pool = the HBM left after the
+    weights.  Layer l's matrices are one seeded draw with rows rotated by l;
+    the KV cache starts as bf16 1.0 everywhere (every read position is written
+    by the loop before it is read)."""
+    from chunked_prefill_hybrid_gb300 import sched, serve
+    L = 60
+    dims = synth.LLAMA_33B.with_layers(L)
+    base = synth.layer_weights(dims, 4 + rank, 0)
+    free, _ = torch.cuda.mem_get_info()
+    w_bytes = L * 2 * sum(v.size for v in base.values())
+    kv_tok = L * 2 * dims.n_kv_heads * dims.head_dim * 2
+    num_blocks = int((free - w_bytes - 14 * 2**30) // (16 * kv_tok))
+    max_pos, max_tokens, max_decodes = 4096, 4096, 512
+    ctx = native.Context(native.model_config(dims, num_blocks, max_tokens, max_decodes, max_pos, n_layers=L))
+    dev = {k: workloads.to_device(v) for k, v in base.items()}
+    for l in range(L):
+        ctx.load_layer(l, {k: (torch.roll(v, l, 0) if v.dim() == 2 else v) for k, v in dev.items()})
+        ctx.sync()
+    del dev, base
+    ctx.fill_kv(0x3F80)
+    x = workloads.to_device(synth.token_rows(4 + rank, (1,), max_tokens, dims.hidden))
+    y = torch.empty_like(x)
+    out = {}
+    for r in [float(v) for v in args.serve_ratios.split(",")]:
+        P = synth.uniform_ints(4 + rank, (2, int(r * 10)), args.serve_requests, 512, 2048)
+        reqs = [(i, int(p), max(1, int(round(p / r)))) for i, p in enumerate(P)]
+        row = {}
+        for name, kw in (("decode_maximal", dict(chunk_size=256, token_budget=512)),
+                         ("request_level", dict(chunk_size=1 << 20, token_budget=max_tokens,
+                                                max_chunks_per_batch=16, max_decodes=max_decodes,
+                                                request_level=1))):
+            s = sched.Scheduler(num_blocks=num_blocks, max_blocks_per_seq=max_pos // 16, **kw)
+            res = serve.run(ctx, s, reqs, x, y)
+            row[name] = res.summary()
+        dm, rl = row["decode_maximal"], row["request_level"]
+        row["throughput_gain"] = dm["tokens_per_s"] / rl["tokens_per_s"]
+        row["decode_throughput_gain"] = dm["decode_tokens_per_s"] / rl["decode_tokens_per_s"]
+        out[f"pd_{r:g}"] = row
+    ctx.free()
+    if rank == 0:
+        print(json.dumps({"serve": "llama33b-60L-c256-budget512", "requests": args.serve_requests,
+                          "kv_blocks": num_blocks, "kv_tokens": num_blocks * 16, "results": out}), flush=True)
+    return 0
+
+
 def sources_sha256(names):
     import hashlib
     h = hashlib.sha256()
@@ -395,6 +445,11 @@ def main():
     ap.add_argument("--tile-curve", action="store_true",
                     help="time the LLaMA-13B hybrid layer against the chunk size (18 decodes at ctx 1024) and print "
                          "one JSON line with the curve instead of the benchmark line")
+    ap.add_argument("--serve", action="store_true",
+                    help="run the LLaMA-33B (60 layers) serving loop, decode-maximal vs the request-level baseline, "
+                         "and print one JSON line with throughput, TTFT/ITL/TPOT and iteration uniformity")
+    ap.add_argument("--serve-requests", type=int, default=128)
+    ap.add_argument("--serve-ratios", default="1,5,10,50", help="P:D ratios r: max_new = max(1, round(P / r))")
     ap.add_argument("--ncu-case", action="store_true",
                     help="run only the warm-up and --steps hybrid steps, untimed (the case ncu captures)")
     args = ap.parse_args()
@@ -412,6 +467,8 @@ def main():
 
     if args.tile_curve:
         return tile_curve(args, torch, native, workloads, synth, world, rank)
+    if args.serve:
+        return serve_bench(args, torch, native, workloads, synth, world, rank)
 
     w = workloads.llama13b_hybrid(seed=2 + rank)
     dims = w.dims

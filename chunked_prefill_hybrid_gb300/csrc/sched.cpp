@@ -53,7 +53,8 @@ extern "C" int hb_sched_create(const hb_sched_config *cfg, hb_sched **out)
         return HB_EINVAL;
     *out = nullptr;
     if (!cfg || cfg->chunk_size <= 0 || cfg->max_decodes < 0 || cfg->tile < 0 || cfg->max_chunks_per_batch < 1 ||
-        cfg->block_size <= 0 || cfg->num_blocks < 0 || cfg->max_blocks_per_seq <= 0)
+        cfg->block_size <= 0 || cfg->num_blocks < 0 || cfg->max_blocks_per_seq <= 0 || cfg->request_level < 0 ||
+        cfg->request_level > 1)
         return HB_EINVAL;
     hb_sched *s = new hb_sched();
     s->cfg = *cfg;
@@ -83,7 +84,11 @@ extern "C" int hb_sched_add(hb_sched *s, int req_id, int prompt_len, int max_new
 
 static void admit(hb_sched *s)
 {
-    while (!s->waiting.empty()) {
+    const bool request_level = s->cfg.request_level != 0;
+    if (request_level && !s->running.empty())
+        return;  // a request-level batch forms only when the previous one has finished
+    const size_t cap = request_level ? (size_t)std::max(1, s->cfg.max_decodes) : (size_t)-1;
+    while (!s->waiting.empty() && s->running.size() < cap) {
         Req &r = s->reqs[s->waiting.front()];
         const int need = blocks_for(s->cfg, (long long)r.prompt + r.max_new);
         if ((int)s->free_blocks.size() < need)
@@ -114,8 +119,14 @@ extern "C" int hb_sched_next(hb_sched *s, hb_sched_batch *out)
     s->d_ids.clear();
     s->d_ctx.clear();
     long long rows = 0;
+    bool prefill_left = false;
+    for (int id : s->running)
+        prefill_left = prefill_left || s->reqs[id].phase == PREFILL;
+    const bool take_decodes = !c.request_level || !prefill_left;
     // decodes first, admission order
     for (int id : s->running) {
+        if (!take_decodes)
+            break;
         const Req &r = s->reqs[id];
         if (r.phase != DECODE)
             continue;

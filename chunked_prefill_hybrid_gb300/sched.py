@@ -14,7 +14,7 @@ from . import native
 class SchedConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("chunk_size", "token_budget", "max_decodes", "tile",
                                              "max_chunks_per_batch", "block_size", "num_blocks",
-                                             "max_blocks_per_seq")]
+                                             "max_blocks_per_seq", "request_level")]
 
 
 class _Batch(ctypes.Structure):
@@ -85,10 +85,10 @@ def advise_chunk(pd_ratio: float, batch_size: int, tile: int = 0, c_min: int = 1
 class Scheduler:
     def __init__(self, chunk_size: int, token_budget: int = 0, max_decodes: int = 1 << 20, tile: int = 0,
                  max_chunks_per_batch: int = 1, block_size: int = 16, num_blocks: int = 1 << 16,
-                 max_blocks_per_seq: int = 1 << 12):
+                 max_blocks_per_seq: int = 1 << 12, request_level: int = 0):
         self.L = _lib()
         self.cfg = SchedConfig(chunk_size, token_budget, max_decodes, tile, max_chunks_per_batch, block_size,
-                               num_blocks, max_blocks_per_seq)
+                               num_blocks, max_blocks_per_seq, int(request_level))
         h = ctypes.c_void_p()
         rc = self.L.hb_sched_create(ctypes.byref(self.cfg), ctypes.byref(h))
         if rc:

@@ -30,6 +30,13 @@
  * tokens produced is finished and its blocks are freed.  Free blocks are
  * handed out lowest id first.
  *
+ * request_level = 1 is the request-level baseline the SARATHI summary compares
+ * against ("Evaluation Methodology", Baselines (1)): prefill-only and
+ * decode-only batches, never mixed.  Requests are admitted only when none is
+ * running, at most max_decodes of them (the batch size B); while any admitted
+ * request has prompt left the batch holds only prefill chunks (steps (3),
+ * (4)); otherwise it holds every running decode (step (2)).
+ *
  * Return codes are those of hb.h.  Pointers returned by the scheduler stay
  * valid until its next call.  Not thread-safe.
  */
@@ -57,6 +64,7 @@ typedef struct {
     int block_size;           /* tokens per KV block (16) */
     int num_blocks;           /* KV blocks the scheduler may hand out */
     int max_blocks_per_seq;   /* table entries per request at most */
+    int request_level;        /* 1: the pages' baseline instead (see below); 0: decode-maximal */
 } hb_sched_config;
 
 typedef struct hb_sched hb_sched;

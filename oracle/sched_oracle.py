@@ -17,6 +17,10 @@ Policy, in the pages' terms:
     Sarathi-Serve", "Stall Free Batching");
   * tile alignment -- with one chunk, shrink it by (rows mod tile) when the
     chunk stays positive (section 3.4, tile quantization: 256 - (B - 1)).
+  * request_level -- the pages' baseline ("Evaluation Methodology",
+    Baselines (1)): prefill-only and decode-only batches, never mixed; a new
+    batch of at most max_decodes requests is admitted only when the last has
+    finished; prefill chunks run while any admitted prompt is unfinished.
 """
 from __future__ import annotations
 
@@ -25,7 +29,7 @@ import math
 
 class SchedOracle:
     def __init__(self, chunk_size, token_budget=0, max_decodes=1 << 20, tile=0, max_chunks_per_batch=1,
-                 block_size=16, num_blocks=1 << 16, max_blocks_per_seq=1 << 12):
+                 block_size=16, num_blocks=1 << 16, max_blocks_per_seq=1 << 12, request_level=0):
         self.C = chunk_size
         self.budget = token_budget if token_budget > 0 else float("inf")
         self.max_decodes = max_decodes
@@ -40,6 +44,7 @@ class SchedOracle:
         self.running = []      # admission order
         self.last = None
         self.pd_ewma = None
+        self.request_level = bool(request_level)
 
     def blocks_needed(self, prompt, max_new):
         return math.ceil((prompt + max_new) / self.bs)
@@ -52,7 +57,11 @@ class SchedOracle:
         self.waiting.append(rid)
 
     def _admit(self):
+        if self.request_level and self.running:
+            return
         while self.waiting:
+            if self.request_level and len(self.running) >= max(1, self.max_decodes):
+                return
             r = self.req[self.waiting[0]]
             need = self.blocks_needed(r["prompt"], r["max_new"])
             if len(self.free) < need:
@@ -66,7 +75,10 @@ class SchedOracle:
         self._admit()
         rows = 0
         decodes = []
+        prefill_left = any(self.req[rid]["phase"] == "prefill" for rid in self.running)
         for rid in self.running:
+            if self.request_level and prefill_left:
+                break
             r = self.req[rid]
             if r["phase"] != "decode":
                 continue

@@ -191,10 +191,6 @@ def test_piggybacked_decode_matches_alone():
         assert ok, (j, st)
 
 
-@pytest.mark.parametrize("impl", [0, 1, 2], ids=["simt", "tcgen05", "pair"])
-@pytest.mark.parametrize("T,N,K", [(1, 256, 256), (18, 768, 256), (68, 1376, 688), (274, 512, 5120),
-                                   (300, 384, 1024), (513, 256, 512), (16, 130, 64), (1100, 640, 192),
-                                   (1500, 384, 128), (2048, 256, 64)])
 def _several_chunks(dims, seed):
     """A Sarathi-Serve batch: the leftover 40 rows of a prompt at offset 24, a new prompt's first 70 rows
     (two 64-row tiles and a tail), a one-row chunk at offset 9, 17 rows at offset 100, and decodes at
@@ -225,6 +221,10 @@ def test_several_chunks_match_oracle(dims, kern):
     ctx.free()
 
 
+@pytest.mark.parametrize("impl", [0, 1, 2], ids=["simt", "tcgen05", "pair"])
+@pytest.mark.parametrize("T,N,K", [(1, 256, 256), (18, 768, 256), (68, 1376, 688), (274, 512, 5120),
+                                   (300, 384, 1024), (513, 256, 512), (16, 130, 64), (1100, 640, 192),
+                                   (1500, 384, 128), (2048, 256, 64)])
 def test_gemm_kernel_against_fp64(impl, T, N, K):
     w = workloads.tiny(seed=1)
     ctx = native.Context(workloads.config(w))

@@ -81,3 +81,38 @@ def test_serving_loop_matches_oracle(mode):
     assert most_chunks == 1 if mode != "multi" else most_chunks > 1
     assert lib.stats()["finished"] == len(reqs)
     ctx.free()
+
+
+@pytest.mark.parametrize("request_level", [0, 1])
+def test_serve_loop_latency_bookkeeping(request_level):
+    """serve.run on a 2-layer tiny model: every request gets exactly max_new token times, in increasing order,
+    the first at its last prompt chunk; decode-maximal batches mix phases, the request-level baseline never does."""
+    from chunked_prefill_hybrid_gb300 import serve
+    seed = 43
+    dims = synth.TINY.with_layers(2)
+    num_blocks, mbs = 256, 32
+    cfg = native.model_config(dims, num_blocks, 256, 64, mbs * 16, n_layers=2)
+    ctx = native.Context(cfg)
+    for l in range(2):
+        ctx.load_layer(l, {k: workloads.to_device(v) for k, v in synth.layer_weights(dims, seed, l).items()})
+    ctx.fill_kv(0x3F80)
+    x = workloads.to_device(synth.token_rows(seed, (1,), 256, dims.hidden))
+    y = torch.empty_like(x)
+    rng = np.random.default_rng(seed)
+    reqs = [(i, int(rng.integers(20, 200)), int(rng.integers(1, 12))) for i in range(24)]
+    kw = dict(chunk_size=64, token_budget=128, num_blocks=num_blocks, max_blocks_per_seq=mbs)
+    if request_level:
+        kw.update(chunk_size=1 << 20, token_budget=256, max_chunks_per_batch=16, max_decodes=8, request_level=1)
+    s = sched.Scheduler(**kw)
+    res = serve.run(ctx, s, reqs, x, y)
+    ctx.free()
+    for rid, p, m in reqs:
+        ts = res.token_times[rid]
+        assert len(ts) == m, (rid, len(ts), m)
+        assert all(b > a for a, b in zip(ts, ts[1:]))
+    mixed = sum(1 for c, d in zip(res.iter_chunks, res.iter_decodes) if c and d)
+    assert (mixed == 0) if request_level else (mixed > 0)
+    sm = res.summary()
+    assert sm["generated_tokens"] == sum(m for _, _, m in reqs)
+    assert sm["iterations"] == len(res.iter_ms) and all(t > 0 for t in res.iter_ms)
+    assert all(b >= a for a, b in zip(res.iter_end_ms, res.iter_end_ms[1:]))

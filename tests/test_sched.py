@@ -130,6 +130,8 @@ CONFIGS = [
     dict(chunk_size=64, tile=32, max_decodes=7),                            # tile alignment
     dict(chunk_size=32, token_budget=40, num_blocks=60),                    # tight KV capacity
     dict(chunk_size=256, token_budget=512, max_chunks_per_batch=1, num_blocks=400),
+    dict(chunk_size=1 << 20, token_budget=256, max_chunks_per_batch=8, max_decodes=6, request_level=1),  # baseline
+    dict(chunk_size=64, max_decodes=4, num_blocks=60, request_level=1),
 ]
 
 
@@ -299,3 +301,33 @@ def test_pd_estimate_tracks_finished_requests(impl):
             break
         s.complete()
     assert abs(est() - 25.625) < 1e-12
+
+
+def test_request_level_baseline_never_mixes_phases():
+    """The request-level baseline ("Evaluation Methodology", Baselines (1)): batches are prefill-only or
+    decode-only, and a new group of at most B requests starts only when the previous group has finished."""
+    lib, orc = both(chunk_size=1 << 20, token_budget=4096, max_chunks_per_batch=16, max_decodes=4, request_level=1)
+    for i in range(10):
+        lib.add(i, 20 + 13 * i, 3 + i % 4)
+        orc.add(i, 20 + 13 * i, 3 + i % 4)
+    groups, live = [], set()
+    while True:
+        b = lib.next()
+        c, d, n = orc.next()
+        assert ([tuple(x) for x in b.chunks], [tuple(x) for x in b.decodes], b.n_rows) == (c, d, n)
+        if b.n_rows == 0:
+            break
+        assert not (b.chunks and b.decodes)
+        ids = {x[0] for x in b.chunks} | {x[0] for x in b.decodes}
+        if not live:
+            groups.append(sorted(ids))
+            live = set(ids)
+        assert ids <= live
+        if b.chunks:   # whole prompts at once
+            assert all(off == 0 for _, off, _ in b.chunks)
+        done_before = lib.stats()["finished"]
+        lib.complete()
+        orc.complete()
+        if lib.stats()["finished"] > done_before:
+            live = {i for i in live if orc.req[i]["phase"] != "done"}
+    assert [len(g) for g in groups] == [4, 4, 2]
