@@ -141,6 +141,23 @@ def test_head_dim_and_gqa_cases(case, dims, kern):
     ctx.free()
 
 
+# an FFN wide enough that the gate/up product (2 x 10240 weight rows = 80 tile pairs) is more than one wave of
+# the GPU's 76 CTA pairs: stream-K over more tiles than pairs, every pair crossing tile boundaries
+WIDE_FFN = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn=10240)
+
+
+@pytest.mark.parametrize("kern", ["pair+hybrid", "tc+hybrid"])
+@pytest.mark.parametrize("case", [(40, 90, [3, 200, 77, 500]), (0, 1, [])], ids=["hybrid", "one_row"])
+def test_wide_ffn_gate_up(case, kern):
+    off, C, ctxs = case
+    w = _tiny(47, off, C, ctxs, dims=WIDE_FFN)
+    ctx, y = run_gpu(w, kernels=KERNELS[kern])
+    ref, pools = oracle_run(w)
+    ok, st = compare(y, ref)
+    assert ok, (kern, st)
+    ctx.free()
+
+
 def test_tiny_gamma_uniform_and_multilayer():
     w = _tiny(12, 40, 50, [10, 70, 130], n_layers=3, gamma="uniform")
     ctx, y = run_gpu(w)
