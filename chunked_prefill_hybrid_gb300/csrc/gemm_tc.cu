@@ -68,6 +68,8 @@ struct TcArgs {
     int *counters;    // [n_mtiles * G]
     const bf16 *w_tiled;  // the weights, streamed into L2 ahead of the TMA loads
     int rel;              // stages released per commit: 2 when the MMAs are short (N < 224), else 1
+    int dp_tiles;         // pair kernel: tile pairs 0..dp_tiles-1 go whole to clusters 0..dp_tiles-1 (fused
+                          // epilogue); units / grid then cover only the stream-K rest, tile pairs dp_tiles..
 };
 
 // A cluster's unit range [u0, u1) is cut at tile boundaries into segments
@@ -107,6 +109,30 @@ struct SegIter {
         else
             t = t0 + i - 1;
         tile_seg(t, a, b);
+    }
+};
+
+// Segments of one pair cluster: with a.dp_tiles > 0, first its whole
+// data-parallel tile pair (if it has one), then its stream-K range [u0, u1)
+// in SegIter order.  get() returns true for the data-parallel segment.
+struct PairSegs {
+    SegIter sk;
+    int n_dp, dp_u0, n;
+    __device__ PairSegs(int clu, const TcArgs &a, int u0, int u1) : sk(u0, u1, a.nkb)
+    {
+        n_dp = clu < a.dp_tiles ? 1 : 0;
+        dp_u0 = clu * a.nkb;
+        n = n_dp + sk.n;
+    }
+    __device__ bool get(int i, int &sa, int &sb) const
+    {
+        if (i < n_dp) {
+            sa = dp_u0;
+            sb = dp_u0 + sk.nkb;
+            return true;
+        }
+        sk.get(i - n_dp, sa, sb);
+        return false;
     }
 };
 
@@ -605,7 +631,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int r = (int)cluster_ctarank();  // 0: the pair's leader
     const int clu = blockIdx.x >> 1;
     const int cta = clu * 2 + r;
-    const int u0 = unit_begin(clu, a), u1 = unit_begin(clu + 1, a);
+    const int sk_base = a.dp_tiles * a.nkb;
+    const int u0 = sk_base + unit_begin(clu, a), u1 = sk_base + unit_begin(clu + 1, a);
     const int rel_mask = a.rel - 1, rel_shift = a.rel == 2 ? 1 : 0;
     pdl_trigger();
 
@@ -643,7 +670,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ------------------------------------------------------ producer
         const uint32_t bytes = (uint32_t)(2 * stage_bytes);  // both CTAs' copies land on the leader's barrier
         const uint64_t wpol = l2_policy_evict_first();
-        const SegIter seg_it(u0, u1, a.nkb);
+        const PairSegs seg_it(clu, a, u0, u1);
         int it = 0, s = 0;
         uint32_t ph = 0;
         bool ok = true, waited = false;
@@ -703,7 +730,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(smem));
             const uint32_t stage16 = (uint32_t)stage_bytes >> 4;
             const uint32_t xsub16 = (uint32_t)(xhalf * TC_BK * 2) >> 4;
-            const SegIter seg_it(u0, u1, a.nkb);
+            const PairSegs seg_it(clu, a, u0, u1);
             int s = 0, slot_next = 0;
             uint32_t ph = 0, st16 = 0, seen = 0, par = 0;
             bool ok = true;
@@ -785,16 +812,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const bool partial_mode = ep.mode == EPI_PARTIAL;
         float *xp = s_xp + q * 32 * TC_XP_LD;
-        const SegIter seg_it(u0, u1, a.nkb);
+        const PairSegs seg_it(clu, a, u0, u1);
         int slot_next = 0;
         for (int seg = 0; seg < seg_it.n; ++seg) {
             int sa, sb;
-            seg_it.get(seg, sa, sb);
+            const bool dp_seg = seg_it.get(seg, sa, sb);
             const int mp = sa / a.nkb, kb0 = sa % a.nkb;
             const int kb1 = kb0 + (sb - sa);
             const int tile = 2 * mp + r;
+            // hybrid launch: the data-parallel tile is finished here, the
+            // stream-K tiles always leave partials for the reduce pass
+            const bool seg_partial = partial_mode || (a.dp_tiles > 0 && !dp_seg);
             const bool whole = (kb0 == 0 && kb1 == a.nkb);
-            const bool direct = whole && !partial_mode;
+            const bool direct = whole && !seg_partial;
             const int nb = tile * TC_BM + q * 32;
             if (direct && ep.mode == EPI_RESID) {
                 for (int c = lane; c < a.tg; c += 32)
@@ -810,7 +840,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int wslot = mp - u0 / a.nkb;
+            const int wslot = dp_seg ? 0 : mp - u0 / a.nkb;
             float *ws_mine = a.ws + ((size_t)cta * a.slots + wslot) * a.tg * TC_BM;
             for (int sub = 0; sub < a.nsub; ++sub) {
                 const int j = slot_next;
@@ -838,7 +868,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (lane == 0)
                     mbar_remote_arrive(sfree_leader + (uint32_t)(j * 8));
             }
-            if (!whole && !partial_mode) {
+            if (!whole && !seg_partial) {
                 __threadfence();
                 epi_bar();
                 const int c_lo = unit_owner((long long)mp * a.nkb, a);
@@ -1016,7 +1046,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf
     const TcShape sh = tc_shape(T);
     if (sh.G > TC_MAX_G)
         return cudaErrorInvalidValue;
-    TcArgs a;
+    TcArgs a = {};
     a.T = T;
     a.N = N;
     a.K = K;
@@ -1149,8 +1179,19 @@ bool tc_pair_data_parallel(const TcRuntime &rt, int N)
     return n_mpairs <= pairs && 10 * n_mpairs >= 6 * pairs;
 }
 
+int tc_pair_dp_tiles(const TcRuntime &rt, int N, int K)
+{
+    const int n_mpairs = ((N + TC_BM - 1) / TC_BM + 1) / 2;
+    const int pairs = rt.num_sms / 2;
+    const long long sk_units = (long long)(n_mpairs - pairs) * ((K + TC_BK - 1) / TC_BK);
+    // every cluster must get stream-K units: the reduce pass sums every
+    // cluster of a tile's contributor range
+    return (n_mpairs > pairs && sk_units >= pairs) ? pairs : 0;
+}
+
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
-                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part, bool pdl)
+                             const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part, bool pdl,
+                             int dp_tiles)
 {
     if (T <= 0)
         return cudaSuccess;
@@ -1173,7 +1214,11 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         return cudaErrorInvalidValue;
     a.wpiece = TC_BM;
     const int n_mpairs = (a.n_mtiles + 1) / 2;
-    const long long units = (long long)n_mpairs * a.nkb;
+    if (dp_tiles < 0 || dp_tiles >= n_mpairs || (dp_tiles > 0 && (ep.mode == EPI_PARTIAL || !part)) ||
+        (dp_tiles > 0 && (long long)(n_mpairs - dp_tiles) * a.nkb < dp_tiles))
+        return cudaErrorInvalidValue;
+    a.dp_tiles = dp_tiles;
+    const long long units = (long long)(n_mpairs - dp_tiles) * a.nkb;  // the stream-K part
     if (units > (1ll << 30) || (long long)n_mpairs * 2 > rt.n_counters)
         return cudaErrorInvalidValue;
     a.units = (int)units;
@@ -1215,7 +1260,13 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         mc = n < rt.num_sms / 2 ? n : rt.num_sms / 2;
     }
     a.grid = tc_grid(units, mc);
-    if (ep.mode != EPI_PARTIAL) {
+    if (dp_tiles > 0) {
+        // one data-parallel wave (tile pair c whole to cluster c, fused
+        // epilogue), then the remaining tile pairs stream-K over all clusters
+        if (dp_tiles > mc)
+            return cudaErrorInvalidValue;
+        a.grid = mc;
+    } else if (ep.mode != EPI_PARTIAL) {
         // data-parallel: one whole weight-tile pair per CTA pair, fused
         // epilogue, no partials
         if (n_mpairs > mc)

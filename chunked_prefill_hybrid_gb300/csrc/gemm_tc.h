@@ -82,9 +82,20 @@ size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, cons
 bool tc_pair_data_parallel(const TcRuntime &rt, int N);
 // pdl: launch with programmatic stream serialization (the weight stream
 // starts while the previous kernel finishes; activations are read after it).
+// dp_tiles > 0 (a fused ep.mode, part given): tile pairs 0..dp_tiles-1 run
+// whole on clusters 0..dp_tiles-1 with the fused epilogue, and the remaining
+// tile pairs run stream-K over every cluster into partials; *part then
+// describes that stream-K part alone (its tile pair 0 is tile pair dp_tiles),
+// for launch_reduce_epi with the epilogue of the features from
+// dp_tiles * 256 on.
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
                              const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr,
-                             bool pdl = false);
+                             bool pdl = false, int dp_tiles = 0);
+// Tile pairs of an N x K product worth running as one data-parallel wave
+// ahead of a stream-K rest: one per CTA pair when the product has more tile
+// pairs than the GPU has CTA pairs and the rest gives every pair at least one
+// k-block; else 0.
+int tc_pair_dp_tiles(const TcRuntime &rt, int N, int K);
 
 // acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
 // tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).

@@ -213,6 +213,17 @@ static cudaError_t launch_attention_tc(const AttnParams &ap, const CUtensorMap &
     return launch_attention_hybrid(ap, s, pdl, true);
 }
 
+// The epilogue parameters of stored output features [n1, N) of a product
+// whose first n1 (a multiple of 256) are finished elsewhere.
+static EpiParams epi_cols(const EpiParams &ep, int n1)
+{
+    EpiParams e = ep;
+    e.N = ep.N - n1;
+    if (e.mode == EPI_SWIGLU)
+        e.act += n1 / 2;  // stored rows 2j, 2j + 1 make feature j
+    return e;
+}
+
 static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X, const bf16 *W, int T, int N, int K,
                         const EpiParams &ep)
 {
@@ -220,6 +231,26 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
         return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
     const int slab = slab_rows(ctx);
     const bool pair = ctx->gemm_impl == 2;
+    // pair kernel on a product of more tile pairs than CTA pairs: one
+    // data-parallel wave with the fused epilogue, the rest stream-K into
+    // partials that a reduce pass finishes (gate/up only: its epilogue maps
+    // stored rows to features by a plain offset, epi_cols)
+    const int dp_tiles = (pair && ep.mode == EPI_SWIGLU) ? tc_pair_dp_tiles(ctx->fast->rt, N, K) : 0;
+    if (dp_tiles > 0) {
+        ctx->n_launches += 2 * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
+        for (int t0 = 0; t0 < T; t0 += slab) {
+            const int Tn = T - t0 < slab ? T - t0 : slab;
+            const EpiParams er = epi_rows(ep, t0, Tn);
+            TcPartition part;
+            cudaError_t e = launch_gemm_pair(M.m[kind][0], W, X + (size_t)t0 * K, Tn, N, K, er, ctx->fast->rt,
+                                             ctx->stream, &part, true, dp_tiles);
+            if (e == cudaSuccess)
+                e = launch_reduce_epi(part, epi_cols(er, dp_tiles * 2 * 128), ctx->stream, true);
+            if (e != cudaSuccess)
+                return e;
+        }
+        return cudaSuccess;
+    }
     // the pair kernel leaves fp32 partial tiles; a grid-wide pass sums them
     // and applies the fused epilogue
     const int per_slab = (pair && !tc_pair_data_parallel(ctx->fast->rt, N)) ? 2 : 1;

@@ -141,16 +141,20 @@ def test_head_dim_and_gqa_cases(case, dims, kern):
     ctx.free()
 
 
-# an FFN wide enough that the gate/up product (2 x 10240 weight rows = 80 tile pairs) is more than one wave of
-# the GPU's 76 CTA pairs: stream-K over more tiles than pairs, every pair crossing tile boundaries
-WIDE_FFN = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn=10240)
+# FFNs wide enough that the gate/up product is more than one wave of the GPU's 76 CTA pairs: 2 x 10752 weight rows
+# = 84 tile pairs at hidden 1024 run as one data-parallel wave with the fused SwiGLU plus 8 tile pairs stream-K
+# (128 k-blocks over 76 pairs) and a reduce pass; 2 x 10240 rows = 80 tile pairs at hidden 256 (16 k-blocks left)
+# run stream-K throughout
+WIDE_FFN = synth.ModelDims(hidden=1024, n_heads=8, n_kv_heads=8, head_dim=128, ffn=10752)
+WIDE_FFN_SK = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn=10240)
 
 
 @pytest.mark.parametrize("kern", ["pair+hybrid", "tc+hybrid"])
+@pytest.mark.parametrize("dims", [WIDE_FFN, WIDE_FFN_SK], ids=["dp_wave", "stream_k"])
 @pytest.mark.parametrize("case", [(40, 90, [3, 200, 77, 500]), (0, 1, [])], ids=["hybrid", "one_row"])
-def test_wide_ffn_gate_up(case, kern):
+def test_wide_ffn_gate_up(case, dims, kern):
     off, C, ctxs = case
-    w = _tiny(47, off, C, ctxs, dims=WIDE_FFN)
+    w = _tiny(47, off, C, ctxs, dims=dims)
     ctx, y = run_gpu(w, kernels=KERNELS[kern])
     ref, pools = oracle_run(w)
     ok, st = compare(y, ref)
