@@ -366,6 +366,9 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
             LK(K_ATTENTION, launch_attention_tc(ap, f->kv_maps[2 * l], f->kv_maps[2 * l + 1], s, pdl));
         else
             LK(K_ATTENTION, launch_attention_hybrid(ap, s, pdl));
+        // LK counted one: the chunk tiles and the decode splits are separate kernels
+        if (f->n_chunk_items > 0 && f->n_items > f->n_chunk_items)
+            ctx->n_launches++;
     } else {
         LK(K_ATTENTION,
            launch_attention_simple(ctx->q, L.k_pool, L.v_pool, b, c.n_heads, c.n_kv_heads, d, ctx->attn_o, s));
