@@ -368,6 +368,62 @@ def serve_bench(args, torch, native, workloads, synth, world, rank):
     return 0
 
 
+def stack_bench(args, torch, native, workloads, synth, world, rank):
+    """LLaMA-13B, all 40 layers: one hybrid iteration (chunk C at offset 768 +
+    D decodes with contexts uniform in [128, 2048]) against a decode-only
+    iteration of the same D decodes, for C in {128, 256, 512} and D from 1 to
+    128; per-layer and whole-stack device time.  Layer l's matrices are one
+    seeded draw with rows rotated by l; the KV cache holds bf16 1.0 (its values
+    do not change the work)."""
+    L = 40
+    dims = synth.LLAMA_13B.with_layers(L)
+    chunks, decodes = [128, 256, 512], [1, 8, 18, 32, 64, 128]
+    dmax, cmax, off = max(decodes), max(chunks), 768
+    ctxs = [int(c) for c in synth.uniform_ints(11 + rank, (9,), dmax, 128, 2048)]
+    lengths = [off + cmax] + [c + 1 for c in ctxs]
+    nb = sum(synth.blocks_needed(n) for n in lengths) + 8
+    batch = synth.hybrid_batch(11 + rank, (7,), off, cmax, ctxs, nb)
+    ctx = native.Context(native.model_config(dims, nb, cmax + dmax, dmax, max(lengths), n_layers=L))
+    base = synth.layer_weights(synth.LLAMA_13B, 11 + rank, 0)
+    dev = {k: workloads.to_device(v) for k, v in base.items()}
+    for l in range(L):
+        ctx.load_layer(l, {k: (torch.roll(v, l, 0) if v.dim() == 2 else v) for k, v in dev.items()})
+        ctx.sync()
+    del dev, base
+    ctx.fill_kv(0x3F80)
+    x = workloads.to_device(synth.token_rows(11 + rank, (8,), cmax + dmax, dims.hidden))
+    y = torch.empty_like(x)
+    steps = max(5, min(args.steps, 20))
+
+    def timed(b):
+        spec = native.Spec(b)
+        for _ in range(3):
+            ctx.forward(spec, x, y)
+        ctx.sync()
+        return max_over_ranks(world, time_steps(torch, ctx, lambda: ctx.forward(spec, x, y), steps, world)) / steps
+
+    out = {"decode_only": {}, "hybrid": {}}
+    for D in decodes:
+        ms = timed(synth.HybridBatch(None, 0, batch.decodes[:D]))
+        out["decode_only"][str(D)] = {"stack_ms": ms, "layer_us": ms / L * 1e3, "decode_tok_s": D / ms * 1e3}
+    for C in chunks:
+        ms_c = timed(synth.HybridBatch(batch.chunk, C, []))
+        row = {"chunk_alone_stack_ms": ms_c}
+        for D in decodes:
+            ms = timed(synth.HybridBatch(batch.chunk, C, batch.decodes[:D]))
+            marg = ms - ms_c
+            dec = out["decode_only"][str(D)]["stack_ms"]
+            row[str(D)] = {"stack_ms": ms, "layer_us": ms / L * 1e3, "tokens_s": (C + D) / ms * 1e3,
+                           "piggybacked_decode_tok_s": D / marg * 1e3 if marg > 0 else None,
+                           "per_decode_cost_ratio": dec / marg if marg > 0 else None}
+        out["hybrid"][str(C)] = row
+    ctx.free()
+    if rank == 0:
+        print(json.dumps({"stack": "llama13b-40L-hybrid", "chunk_offset": off, "decode_ctx": "U[128,2048]",
+                          "steps_timed": steps, "kv_blocks": nb, "results": out}), flush=True)
+    return 0
+
+
 def sources_sha256(names):
     import hashlib
     h = hashlib.sha256()
@@ -445,6 +501,9 @@ def main():
     ap.add_argument("--tile-curve", action="store_true",
                     help="time the LLaMA-13B hybrid layer against the chunk size (18 decodes at ctx 1024) and print "
                          "one JSON line with the curve instead of the benchmark line")
+    ap.add_argument("--stack", action="store_true",
+                    help="time the full LLaMA-13B stack (40 layers): hybrid batches of chunk C in {128, 256, 512} "
+                         "+ D decodes against decode-only batches of the same D; one JSON line")
     ap.add_argument("--serve", action="store_true",
                     help="run the LLaMA-33B (60 layers) serving loop, decode-maximal vs the request-level baseline, "
                          "and print one JSON line with throughput, TTFT/ITL/TPOT and iteration uniformity")
@@ -469,6 +528,8 @@ def main():
         return tile_curve(args, torch, native, workloads, synth, world, rank)
     if args.serve:
         return serve_bench(args, torch, native, workloads, synth, world, rank)
+    if args.stack:
+        return stack_bench(args, torch, native, workloads, synth, world, rank)
 
     w = workloads.llama13b_hybrid(seed=2 + rank)
     dims = w.dims

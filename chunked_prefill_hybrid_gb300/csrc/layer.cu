@@ -167,7 +167,15 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
 // Largest token slab of one tensor-core GEMM launch (8 token groups of 256).
 constexpr int kSlab = 2048;  // rows per launch of the token-group kernel
 // rows per launch of the selected tensor-core kernel
-static int slab_rows(const hb_ctx *ctx) { return ctx->gemm_impl == 2 ? TC_PAIR_MAX_T : kSlab; }
+// rows per launch of the selected tensor-core kernel for a batch of T rows:
+// the fewest launches, with their rows balanced (each launch streams the
+// weights once, so 513 rows run as 257 + 256 rather than 512 + 1)
+static int slab_rows(const hb_ctx *ctx, int T)
+{
+    const int mx = ctx->gemm_impl == 2 ? TC_PAIR_MAX_T : kSlab;
+    const int n = (T + mx - 1) / mx;
+    return n > 1 ? (T + n - 1) / n : mx;
+}
 
 // One launch of the selected tensor-core kernel (token groups or CTA pairs).
 static cudaError_t launch_tc(const hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *W, const bf16 *X, int T,
@@ -229,7 +237,7 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
 {
     if (ctx->gemm_impl == 0)
         return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
-    const int slab = slab_rows(ctx);
+    const int slab = slab_rows(ctx, T);
     const bool pair = ctx->gemm_impl == 2;
     // pair kernel on a product of more tile pairs than CTA pairs: one
     // data-parallel wave with the fused epilogue, the rest stream-K into
@@ -285,7 +293,7 @@ static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const 
                                int K, const bf16 *resid, bf16 *out, const float *gamma, bf16 *norm_out, int *launches)
 {
     const hb_model_config &c = ctx->cfg;
-    const int slab = slab_rows(ctx);
+    const int slab = slab_rows(ctx, T);
     for (int t0 = 0; t0 < T; t0 += slab) {
         const int Tn = T - t0 < slab ? T - t0 : slab;
         EpiParams pp{};
