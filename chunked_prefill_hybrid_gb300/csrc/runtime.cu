@@ -404,6 +404,11 @@ extern "C" int hb_init(const hb_model_config *cfg, const hb_layer_weights *weigh
     ctx->meta_cap = 3 * MT + 4 * max_seq + max_seq * c.max_blocks_per_seq + kMetaExtraWords(c);
     if ((rc = ctx_alloc(ctx, (void **)&ctx->d_meta, ctx->meta_cap * sizeof(int))))
         return bail(rc);
+    if (cudaMallocHost((void **)&ctx->h_err, sizeof(int)) != cudaSuccess) {
+        ctx->h_err = nullptr;
+        return bail(HB_ENOMEM);
+    }
+    *ctx->h_err = 0;
     for (int i = 0; i < kMetaRing; ++i) {
         if (cudaMallocHost((void **)&ctx->h_meta[i], ctx->meta_cap * sizeof(int)) != cudaSuccess) {
             ctx->h_meta[i] = nullptr;
@@ -632,9 +637,10 @@ extern "C" int hb_sync(hb_ctx *ctx)
 {
     if (!ctx)
         return HB_EINVAL;
+    // the error word comes back on the stream, after its work: one wait
+    CK(cudaMemcpyAsync(ctx->h_err, ctx->err_word, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
-    int w = 0;
-    CK(cudaMemcpy(&w, ctx->err_word, sizeof(int), cudaMemcpyDeviceToHost));
+    const int w = *ctx->h_err;
     if (w) {
         CK(cudaMemset(ctx->err_word, 0, sizeof(int)));
         return ctx->set_error(HB_EDEVICE, "device error word = %d (%s)", w,
@@ -720,6 +726,8 @@ extern "C" void hb_free(hb_ctx *ctx)
     hb_free_fast_path(ctx);
     for (void *p : ctx->allocations)
         cudaFree(p);
+    if (ctx->h_err)
+        cudaFreeHost(ctx->h_err);
     for (int i = 0; i < kMetaRing; ++i) {
         if (ctx->h_meta[i])
             cudaFreeHost(ctx->h_meta[i]);

@@ -76,6 +76,7 @@ struct hb_ctx {
     hb::bf16 *xn = nullptr, *q = nullptr, *attn_o = nullptr, *h = nullptr, *act = nullptr;
     hb::bf16 *xa = nullptr, *xb = nullptr, *host_in = nullptr, *host_out = nullptr;
     int *err_word = nullptr;
+    int *h_err = nullptr;  // pinned: the error word read back with the stream's work
 
     // batch metadata: pinned staging ring + one device buffer
     int *d_meta = nullptr;
