@@ -68,6 +68,7 @@ struct TcArgs {
     int *counters;    // [n_mtiles * G]
     const bf16 *w_tiled;  // the weights, streamed into L2 ahead of the TMA loads
     int rel;              // stages released per commit: 2 when the MMAs are short (N < 224), else 1
+    int qkv_smem;         // pair kernel, whole QKV tiles: stage the RoPE'd tile in shared memory, store coalesced
     int dp_tiles;         // pair kernel: tile pairs 0..dp_tiles-1 go whole to clusters 0..dp_tiles-1 (fused
                           // epilogue); units / grid then cover only the stream-K rest, tile pairs dp_tiles..
 };
@@ -577,6 +578,123 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 }
 
+// QKV epilogue of a whole tile staged in shared memory (the pipeline stages
+// are idle once the tile's last MMA has completed), so that the stores to q
+// and to the KV pool are whole head rows instead of 16-byte pieces of 32
+// different rows.  qkv_cols_to_smem is emit_cols for EPI_QKV with the same
+// arithmetic, writing token t's rotated features into row t of tile_s
+// ([tg][QKV_TS] bf16, rows padded by 16 bytes so the 16-row column writes do
+// not share banks); qkv_tile_out then copies row by row, 16 bytes a thread.
+constexpr int QKV_TS = TC_BM + 8;  // bf16 per staged token row
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, const uint4 &v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void qkv_cols_to_smem(const EpiParams &p, const int *s_pos, float *xp, int col0, int ncol,
+                                                 int nb, int tile, int lane, const uint32_t (&r)[32], uint32_t tile_s)
+{
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        xp[j * TC_XP_LD + lane] = __uint_as_float(r[j]);  // row = token, column = feature
+    __syncwarp();
+    const int g = lane & 1;
+    const int n0 = nb + g * 16;
+    const int d = p.head_dim, half = d >> 1;
+    const int hb = n0 / d, i0 = (n0 % d) >> 1;
+    const int lf = (n0 - tile * TC_BM) / d * d + i0;  // feature of the lo half within the tile row
+    const bool rot = hb < p.n_heads + p.n_kv;
+    int c[2];
+    bool ok[2];
+    float v[2][16];
+    float4 cs[2][4];
+    // both groups' (cos, sin) loads are issued before any store, and the next
+    // chunk's lines are pulled into L1 meanwhile
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int j = (lane >> 1) + 16 * k;
+        c[k] = col0 + j;
+        ok[k] = j < ncol && c[k] < p.T && n0 < p.N;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            v[k][e] = xp[j * TC_XP_LD + g * 16 + e];
+        if (ok[k])
+            qkv_rope_load(p, s_pos[c[k]], n0, cs[k]);
+    }
+    if (rot) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int cn = c[k] + 32;
+            if (cn < p.T)
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(p.rope + (size_t)s_pos[cn] * half + i0));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if (!ok[k])
+            continue;
+        float lo[8], hi[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            lo[q] = v[k][2 * q];
+            hi[q] = v[k][2 * q + 1];
+        }
+        if (rot) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 cc = cs[k][q];
+                const float x0 = lo[2 * q], x1 = hi[2 * q], y0 = lo[2 * q + 1], y1 = hi[2 * q + 1];
+                lo[2 * q] = x0 * cc.x - x1 * cc.y;
+                hi[2 * q] = x1 * cc.x + x0 * cc.y;
+                lo[2 * q + 1] = y0 * cc.z - y1 * cc.w;
+                hi[2 * q + 1] = y1 * cc.z + y0 * cc.w;
+            }
+        }
+        const uint32_t row = tile_s + 2u * (uint32_t)(c[k] * QKV_TS);
+        sts_v4(row + 2u * (uint32_t)lf, pack8_bf16(lo));
+        sts_v4(row + 2u * (uint32_t)(lf + half), pack8_bf16(hi));
+    }
+}
+
+__device__ __forceinline__ void qkv_tile_out(const EpiParams &p, uint32_t s_slot, uint32_t tile_s, int tile, int et)
+{
+    const int d = p.head_dim;
+    const int lvec = d == 128 ? 4 : 3;  // log2 of the 16-byte vectors per head row (d = 128 or 64)
+    const int v16 = et & 15;            // this thread's vector of the tile's 128-feature row
+    const int hh = v16 >> lvec, v = v16 & ((1 << lvec) - 1);
+    const int hb = tile * TC_BM / d + hh;
+    if (hb >= p.n_heads + 2 * p.n_kv)
+        return;  // rows past N
+    const bool is_q = hb < p.n_heads, is_k = hb < p.n_heads + p.n_kv;
+    const int kvh = is_k ? hb - p.n_heads : hb - p.n_heads - p.n_kv;
+    bf16 *const qbase = p.q_out + (size_t)hb * d + v * 8;
+    bf16 *const pool = (is_k ? p.k_pool : p.v_pool) + (size_t)kvh * 16 * d + v * 8;
+    for (int t = et >> 4; t < p.T; t += 8) {
+        uint32_t x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                     : "r"(tile_s + 2u * (uint32_t)(t * QKV_TS + v16 * 8)));
+        bf16 *dst;
+        if (is_q) {
+            dst = qbase + (size_t)t * p.n_heads * d;
+        } else {
+            int sl;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sl) : "r"(s_slot + 4u * (uint32_t)t));
+            const int blk = sl >> 4, off = sl & 15;
+            if (blk < 0 || blk >= p.num_blocks) {
+                set_dev_err(p.err, DERR_BAD_SLOT);
+                continue;
+            }
+            dst = pool + ((size_t)blk * p.n_kv * 16 + off) * d;
+        }
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(x0), "r"(x1), "r"(x2), "r"(x3)
+                     : "memory");
+    }
+}
+
 // ------------------------------------------------------------ pair kernel
 // The same linear op on CTA pairs (clusters of two) with the 2-SM MMA: one
 // tcgen05.mma.cta_group::2 computes a 256-row x n_sub-token product whose
@@ -825,6 +943,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const bool seg_partial = partial_mode || (a.dp_tiles > 0 && !dp_seg);
             const bool whole = (kb0 == 0 && kb1 == a.nkb);
             const bool direct = whole && !seg_partial;
+            // the CTA's last segment: no copy into the stages is pending once its accumulator is full
+            const bool staged = direct && a.qkv_smem && seg == seg_it.n - 1;
             const int nb = tile * TC_BM + q * 32;
             if (direct && ep.mode == EPI_RESID) {
                 for (int c = lane; c < a.tg; c += 32)
@@ -840,6 +960,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            if (staged)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stages' async-proxy use is over
             const int wslot = dp_seg ? 0 : mp - u0 / a.nkb;
             float *ws_mine = a.ws + ((size_t)cta * a.slots + wslot) * a.tg * TC_BM;
             for (int sub = 0; sub < a.nsub; ++sub) {
@@ -853,7 +975,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tmem_ld_wait();
                     const int col0 = sub * a.n_sub + c0;
                     const int ncol = min(32, a.n_sub - c0);
-                    if (direct) {
+                    if (staged) {
+                        qkv_cols_to_smem(ep, s_pos, xp, col0, ncol, nb, tile, lane, rr, smem_u32(smem));
+                    } else if (direct) {
                         emit_cols(ep, s_pos, s_slot, xp, 0, col0, ncol, nb, lane, rr);
                     } else {
 #pragma unroll
@@ -867,6 +991,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_remote_arrive(sfree_leader + (uint32_t)(j * 8));
+            }
+            if (staged) {
+                epi_bar();  // the whole tile is in shared memory
+                qkv_tile_out(ep, smem_u32(s_slot), smem_u32(smem), tile, et);
             }
             if (!whole && !seg_partial) {
                 __threadfence();
@@ -1272,6 +1400,10 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         if (n_mpairs > mc)
             return cudaErrorInvalidValue;
         a.grid = n_mpairs;
+        a.qkv_smem = (ep.mode == EPI_QKV && (ep.head_dim == 128 || ep.head_dim == 64) &&
+                      (long long)a.tg * QKV_TS * 2 <= (long long)stages * pair_stage_bytes(a.nsub, a.n_sub))
+                         ? 1
+                         : 0;
     }
     a.slots = tc_slots(units, a.grid, a.nkb);
     if ((size_t)a.grid * 2 * a.slots * a.tg * TC_BM > rt.ws_floats)
