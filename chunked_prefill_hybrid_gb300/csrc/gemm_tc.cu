@@ -116,6 +116,8 @@ struct SegIter {
 // Segments of one pair cluster: with a.dp_tiles > 0, first its whole
 // data-parallel tile pair (if it has one), then its stream-K range [u0, u1)
 // in SegIter order.  get() returns true for the data-parallel segment.
+// (Measured: the other order, which frees the stages for a staged SwiGLU
+// epilogue of the data-parallel tile, is slower.)
 struct PairSegs {
     SegIter sk;
     int n_dp, dp_u0, n;
@@ -672,26 +674,42 @@ __device__ __forceinline__ void qkv_tile_out(const EpiParams &p, uint32_t s_slot
     const int kvh = is_k ? hb - p.n_heads : hb - p.n_heads - p.n_kv;
     bf16 *const qbase = p.q_out + (size_t)hb * d + v * 8;
     bf16 *const pool = (is_k ? p.k_pool : p.v_pool) + (size_t)kvh * 16 * d + v * 8;
-    for (int t = et >> 4; t < p.T; t += 8) {
-        uint32_t x0, x1, x2, x3;
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                     : "r"(tile_s + 2u * (uint32_t)(t * QKV_TS + v16 * 8)));
-        bf16 *dst;
-        if (is_q) {
-            dst = qbase + (size_t)t * p.n_heads * d;
-        } else {
-            int sl;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sl) : "r"(s_slot + 4u * (uint32_t)t));
-            const int blk = sl >> 4, off = sl & 15;
-            if (blk < 0 || blk >= p.num_blocks) {
-                set_dev_err(p.err, DERR_BAD_SLOT);
-                continue;
+    // four tokens per round: their loads are issued before their stores
+    for (int t0 = et >> 4; t0 < p.T; t0 += 32) {
+        uint4 val[4];
+        int sl[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + 8 * u;
+            if (t < p.T) {
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(val[u].x), "=r"(val[u].y), "=r"(val[u].z), "=r"(val[u].w)
+                             : "r"(tile_s + 2u * (uint32_t)(t * QKV_TS + v16 * 8)));
+                sl[u] = 0;
+                if (!is_q)
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sl[u]) : "r"(s_slot + 4u * (uint32_t)t));
             }
-            dst = pool + ((size_t)blk * p.n_kv * 16 + off) * d;
         }
-        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(x0), "r"(x1), "r"(x2), "r"(x3)
-                     : "memory");
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = t0 + 8 * u;
+            if (t >= p.T)
+                continue;
+            bf16 *dst;
+            if (is_q) {
+                dst = qbase + (size_t)t * p.n_heads * d;
+            } else {
+                const int blk = sl[u] >> 4, off = sl[u] & 15;
+                if (blk < 0 || blk >= p.num_blocks) {
+                    set_dev_err(p.err, DERR_BAD_SLOT);
+                    continue;
+                }
+                dst = pool + ((size_t)blk * p.n_kv * 16 + off) * d;
+            }
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(val[u].x), "r"(val[u].y),
+                         "r"(val[u].z), "r"(val[u].w)
+                         : "memory");
+        }
     }
 }
 
