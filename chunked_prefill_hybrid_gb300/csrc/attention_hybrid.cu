@@ -337,12 +337,16 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
     }
     __syncthreads();
 
+    // a decode's K/V is read once per step: evict-first keeps it from pushing
+    // the weights and activations of the neighbouring kernels out of L2
+    uint64_t kv_pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_pol));
     auto issue = [&](int i) {
         const int s = i % NSTAGE;
         const size_t off = (((size_t)bt[b0 + i] * p.n_kv + kvh) * 16) * D;
         mbar_expect_tx(&full[s], STG);
-        bulk_load(ring + s * STG, p.k_pool + off, BLK, &full[s]);
-        bulk_load(ring + s * STG + BLK, p.v_pool + off, BLK, &full[s]);
+        bulk_load_hint(ring + s * STG, p.k_pool + off, BLK, &full[s], kv_pol);
+        bulk_load_hint(ring + s * STG + BLK, p.v_pool + off, BLK, &full[s], kv_pol);
     };
     if (lane == 0)
         for (int i = warp; i < min(nb, NSTAGE); i += 4)

@@ -130,6 +130,17 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// The same with an L2 cache policy (createpolicy) for the source lines.
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // ------------------------------------------------- warp-wide issue helpers
 // The producer and MMA roles run their loops on a whole converged warp, so
 // every address, coordinate and descriptor is warp-uniform and the compiler
