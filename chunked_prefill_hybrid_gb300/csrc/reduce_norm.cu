@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(1024) k_reduce_norm(RnArgs a)
 // for the QKV projection, SwiGLU for gate/up).
 constexpr int RE_THREADS = 256;
 
-__global__ void __launch_bounds__(RE_THREADS) k_reduce_epi(TcPartition p, EpiParams ep)
+__global__ void __launch_bounds__(RE_THREADS, 4) k_reduce_epi(TcPartition p, EpiParams ep)
 {
     __shared__ RdTab tab;
     pdl_trigger();
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(RE_THREADS) k_reduce_epi(TcPartition p, EpiPar
     const int n0 = (blockIdx.y * RE_THREADS + threadIdx.x) * 16;
     if (n0 < ep.N) {
         float v[16];
-        rd_sum<16, 4>(p, tab, t, n0, v);
+        rd_sum<16, 2>(p, tab, t, n0, v);
         epi_group(ep, t, n0, v);
     }
 }
