@@ -313,13 +313,15 @@ static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const 
     return cudaSuccess;
 }
 
-// One decoder layer.  On the tensor-core path the QKV and gate/up GEMMs
-// apply their epilogues (RoPE + KV append, SwiGLU) themselves; the O-proj
-// and down-proj GEMMs leave split-K partials that one kernel per token row
-// finishes with the residual add and the next RMSNorm.  A layer is 7
-// launches: [norm-1 for the first layer only], QKV GEMM, attention, O GEMM,
-// reduce + residual + norm-2, gate/up GEMM, down GEMM, reduce + residual
-// (+ norm-1 of the next layer).
+// One decoder layer.  On the tensor-core path the QKV GEMM applies RoPE and
+// the KV append in its own epilogue; the gate/up GEMM applies SwiGLU to its
+// data-parallel wave and leaves stream-K partials for the rest, which a
+// reduce pass finishes with SwiGLU; the O-proj and down-proj GEMMs leave
+// stream-K partials that one kernel per token row finishes with the
+// residual add and the next RMSNorm.  With the pair kernel a LLaMA-13B layer
+// is 10 kernels: [norm-1 for the first layer only], QKV GEMM, chunk and
+// decode attention, O GEMM, reduce + residual + norm-2, gate/up GEMM, its
+// reduce, down GEMM, reduce + residual (+ norm-1 of the next layer).
 int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, const bf16 *x, bf16 *y)
 {
     const hb_model_config &c = ctx->cfg;

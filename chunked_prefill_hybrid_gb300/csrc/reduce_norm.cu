@@ -1,6 +1,6 @@
-// reduce_norm.cu -- finishes the split-K linear ops whose partial tiles the
-// tensor-core GEMM left in its workspace (O-proj and down-proj), fused with
-// the residual add and the next RMSNorm:
+// reduce_norm.cu -- finishes the stream-K linear ops whose partial tiles the
+// tensor-core GEMM left in its workspace.  k_reduce_norm (O-proj and
+// down-proj) fuses the residual add and the next RMSNorm:
 //   out[t]  = bf16(resid[t] + sum of the partial tiles, in CTA order)
 //   norm[t] = bf16(out[t] * rsqrt(mean(out[t]^2) + eps) * gamma)   (optional)
 // One CTA per token row; each thread owns groups of 8 consecutive features
@@ -141,9 +141,10 @@ __global__ void __launch_bounds__(1024) k_reduce_norm(RnArgs a)
     }
 }
 
-// Generic finish: every 16-feature group of row t is the sum of its
-// contributors' partials, handed to the fused epilogue (RoPE + KV append
-// for the QKV projection, SwiGLU for gate/up).
+// Generic finish (k_reduce_epi): every 16-feature group of row t is the sum
+// of its contributors' partials, handed to the fused epilogue (SwiGLU for
+// the stream-K tail of gate/up; RoPE + KV append when a QKV projection runs
+// stream-K; plain fp32 for the GEMM test hook).
 constexpr int RE_THREADS = 256;
 
 __global__ void __launch_bounds__(RE_THREADS, 4) k_reduce_epi(TcPartition p, EpiParams ep)
