@@ -33,6 +33,11 @@
 //               epilogue on (token, 16 features) with 16-byte accesses
 // Every mbarrier wait is bounded (wall clock); on a timeout the kernel
 // records an error in the device error word, drains and frees TMEM.
+//
+// That is k_gemm_tc, the token-group kernel.  The default is k_gemm_pair
+// further down: the same product on CTA pairs with the 2-SM MMA, data-
+// parallel, stream-K or one data-parallel wave plus a stream-K tail; its own
+// comment describes it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
