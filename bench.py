@@ -226,6 +226,19 @@ def oracle_sample(w, target_s: float):
     return n / dt, n, dt, threads
 
 
+def oracle_one_core(w, target_s: float):
+    """The oracle on one thread over a bounded sample (first chunk rows and
+    first decodes, about target_s seconds); returns (rows_per_s, rows, s)."""
+    from oracle import oracle as orc
+    threads = orc.max_threads()
+    orc.set_threads(1)
+    try:
+        rps, n, dt, _ = oracle_sample(w, target_s)
+    finally:
+        orc.set_threads(threads)
+    return rps, n, dt
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle on the host cores, same workload."""
     world, rank, local = dist_init(args.gpus)
@@ -249,7 +262,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "layers": 1, "T": w.T},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "one_core": dict(zip(("value", "rows", "seconds"),
+                                                                    oracle_one_core(w, args.ref_seconds / 3)))},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -628,6 +642,9 @@ def main():
         line["cpu_baseline"] = {"value": rps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{n} of {w.T} rows (first chunk rows + first decodes), one layer, "
                                           f"fp64 mirror mode, {dt:.1f} s"}
+        r1, n1, dt1 = oracle_one_core(w, target_s=3.0)
+        line["cpu_baseline"]["one_core"] = {"value": r1, "unit": "tokens/s", "cores": 1,
+                                            "sample": f"{n1} rows, {dt1:.1f} s"}
     ctx.free()
     if rank == 0:
         print(json.dumps(line), flush=True)
