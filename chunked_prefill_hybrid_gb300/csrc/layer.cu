@@ -166,7 +166,6 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
 
 // Largest token slab of one tensor-core GEMM launch (8 token groups of 256).
 constexpr int kSlab = 2048;  // rows per launch of the token-group kernel
-// rows per launch of the selected tensor-core kernel
 // rows per launch of the selected tensor-core kernel for a batch of T rows:
 // the fewest launches, with their rows balanced (each launch streams the
 // weights once, so 513 rows run as 257 + 256 rather than 512 + 1)
