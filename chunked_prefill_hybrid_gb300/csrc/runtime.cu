@@ -565,7 +565,10 @@ static int upload_plan(hb_ctx *ctx, const Plan &p, BatchDev &b)
     return HB_OK;
 }
 
-static int run_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, const void *x_in, void *x_out)
+// Validates the call, plans the batch into ctx->plan and uploads the plan's
+// device metadata (stream-ordered before any later launch).
+static int prepare_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, const void *x_in, const void *x_out,
+                          BatchDev &b)
 {
     if (!ctx)
         return HB_EINVAL;
@@ -582,15 +585,18 @@ static int run_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, co
     int rc = plan_batch(c, spec, p, &e);
     if (rc)
         return ctx->set_error(rc, "%s", e.c_str());
-    const int T = p.T;
-    const size_t xbytes = (size_t)T * c.hidden * sizeof(bf16);
+    const size_t xbytes = (size_t)p.T * c.hidden * sizeof(bf16);
     const char *xi = (const char *)x_in;
-    char *xo = (char *)x_out;
+    const char *xo = (const char *)x_out;
     if (xi < xo + xbytes && xo < xi + xbytes)
         return ctx->set_error(HB_EINVAL, "x_in and x_out overlap");
-    BatchDev b;
-    if ((rc = upload_plan(ctx, p, b)))
-        return rc;
+    return upload_plan(ctx, p, b);
+}
+
+// Launches layers [l0, l1) of the prepared batch.
+static int launch_layers(hb_ctx *ctx, const BatchDev &b, int l0, int l1, const void *x_in, void *x_out)
+{
+    int rc;
     const bf16 *x = (const bf16 *)x_in;
     for (int l = l0; l < l1; ++l) {
         bf16 *y = (l == l1 - 1) ? (bf16 *)x_out : ((l - l0) % 2 == 0 ? ctx->xa : ctx->xb);
@@ -599,6 +605,13 @@ static int run_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, co
         x = y;
     }
     return HB_OK;
+}
+
+static int run_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1, const void *x_in, void *x_out)
+{
+    BatchDev b;
+    const int rc = prepare_layers(ctx, spec, l0, l1, x_in, x_out, b);
+    return rc ? rc : launch_layers(ctx, b, l0, l1, x_in, x_out);
 }
 
 extern "C" int hb_forward(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in, void *x_out)
@@ -620,14 +633,13 @@ extern "C" int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const voi
         return HB_EINVAL;
     if (!x_in_host || !x_out_host)
         return ctx->set_error(HB_EINVAL, "NULL host buffer");
-    std::string e;
-    Plan tmp;
-    int rc = plan_batch(ctx->cfg, spec, tmp, &e);
+    BatchDev b;
+    int rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out, b);
     if (rc)
-        return ctx->set_error(rc, "%s", e.c_str());
-    const size_t bytes = (size_t)tmp.T * ctx->cfg.hidden * sizeof(bf16);
+        return rc;
+    const size_t bytes = (size_t)ctx->plan.T * ctx->cfg.hidden * sizeof(bf16);
     CK(cudaMemcpyAsync(ctx->host_in, x_in_host, bytes, cudaMemcpyHostToDevice, ctx->stream));
-    if ((rc = run_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out)))
+    if ((rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out)))
         return rc;
     CK(cudaMemcpyAsync(x_out_host, ctx->host_out, bytes, cudaMemcpyDeviceToHost, ctx->stream));
     return hb_sync(ctx);
