@@ -73,8 +73,9 @@ int validate_config(const hb_model_config &c, std::string *err)
     return HB_OK;
 }
 
-// Validation and row metadata of one batch (host only, no GPU).
-int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::string *err)
+// The batch's row count T, with the checks on the spec's counts and lengths
+// that fix it (the first part of plan_batch).
+static int spec_rows(const hb_model_config &c, const hb_batch_spec *s, int *rows, std::string *err)
 {
     if (!s)
         return fail(err, HB_EINVAL, "spec is NULL");
@@ -126,6 +127,19 @@ int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::s
         return fail(err, HB_EINVAL, "empty batch (no chunk and no decodes)");
     if (T > c.max_tokens)
         return fail(err, HB_ERANGE, "batch has %lld rows > max_tokens %d", T, c.max_tokens);
+    *rows = (int)T;
+    return HB_OK;
+}
+
+// Validation and row metadata of one batch (host only, no GPU).
+int plan_batch(const hb_model_config &c, const hb_batch_spec *s, Plan &p, std::string *err)
+{
+    int T = 0;
+    if (const int rc = spec_rows(c, s, &T, err))
+        return rc;
+    const bool has_chunk = s->chunk_req_id >= 0;
+    const int n_more = s->n_more_chunks;
+    const int clen = T - s->n_decodes;
     if (s->n_decodes > 0) {
         if (!s->decode_req_ids || !s->decode_ctx_lens || !s->decode_block_tables)
             return fail(err, HB_EINVAL, "decode arrays are NULL");
@@ -633,12 +647,19 @@ extern "C" int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const voi
         return HB_EINVAL;
     if (!x_in_host || !x_out_host)
         return ctx->set_error(HB_EINVAL, "NULL host buffer");
-    BatchDev b;
-    int rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out, b);
+    std::string e;
+    int T = 0;
+    int rc = spec_rows(ctx->cfg, spec, &T, &e);
     if (rc)
-        return rc;
-    const size_t bytes = (size_t)ctx->plan.T * ctx->cfg.hidden * sizeof(bf16);
+        return ctx->set_error(rc, "%s", e.c_str());
+    // the input copy runs while the host plans the batch
+    const size_t bytes = (size_t)T * ctx->cfg.hidden * sizeof(bf16);
     CK(cudaMemcpyAsync(ctx->host_in, x_in_host, bytes, cudaMemcpyHostToDevice, ctx->stream));
+    BatchDev b;
+    if ((rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out, b))) {
+        cudaStreamSynchronize(ctx->stream);  // x_in_host is the caller's again once this returns
+        return rc;
+    }
     if ((rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out)))
         return rc;
     CK(cudaMemcpyAsync(x_out_host, ctx->host_out, bytes, cudaMemcpyDeviceToHost, ctx->stream));

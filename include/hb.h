@@ -169,7 +169,8 @@ int hb_read_kv(hb_ctx *ctx, int layer, const int32_t *block_table, int n_blocks,
 int hb_fill_kv(hb_ctx *ctx, uint16_t bits);
 
 /* Run the batch through all layers.  x_in, x_out: device bf16 [T][hidden],
- * T = chunk_len + n_decodes; they may not overlap.  Each layer writes the
+ * T = chunk_len + the further chunks' lengths + n_decodes; they may not
+ * overlap.  Each layer writes the
  * batch's new K/V into its pool at the rows' slots, then attends.  The
  * library does not advance request lengths; the scheduler does. */
 int hb_forward(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in, void *x_out);
@@ -180,7 +181,11 @@ int hb_forward_layers(hb_ctx *ctx, const hb_batch_spec *spec, int layer_begin, i
 
 /* Like hb_forward, but x_in and x_out are HOST bf16 buffers: the call copies
  * x_in to the device, runs the stack and copies the result back, all on the
- * context's stream, and waits for it.  Use pinned host memory for speed. */
+ * context's stream, and waits for it.  Use pinned host memory for speed.
+ * The input copy starts before the batch is fully validated (it overlaps the
+ * host's planning); when the batch is then rejected, the call waits for that
+ * copy before it returns the error, so x_in_host is free again on return and
+ * x_out_host is untouched. */
 int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in_host, void *x_out_host);
 
 /* Wait for the context's stream; returns HB_EDEVICE if a kernel set the
