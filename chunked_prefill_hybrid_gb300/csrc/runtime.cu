@@ -655,14 +655,27 @@ extern "C" int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const voi
     // the input copy runs while the host plans the batch
     const size_t bytes = (size_t)T * ctx->cfg.hidden * sizeof(bf16);
     CK(cudaMemcpyAsync(ctx->host_in, x_in_host, bytes, cudaMemcpyHostToDevice, ctx->stream));
+    // A page-locked output buffer that the GPU can address is written in
+    // place by the last kernel's stores (every output store is a plain
+    // st.global), so no copy follows the stack; any other buffer gets the
+    // result by a device-to-host copy.
+    void *y_mapped = nullptr;
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, x_out_host) == cudaSuccess) {
+        if (pa.type == cudaMemoryTypeHost && pa.devicePointer)
+            y_mapped = pa.devicePointer;
+    } else {
+        cudaGetLastError();  // not a CUDA-known pointer: clear the error, copy
+    }
+    void *y = y_mapped ? y_mapped : (void *)ctx->host_out;
     BatchDev b;
-    if ((rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out, b))) {
+    if ((rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->host_in, y, b)) ||
+        (rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->host_in, y))) {
         cudaStreamSynchronize(ctx->stream);  // x_in_host is the caller's again once this returns
         return rc;
     }
-    if ((rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->host_in, ctx->host_out)))
-        return rc;
-    CK(cudaMemcpyAsync(x_out_host, ctx->host_out, bytes, cudaMemcpyDeviceToHost, ctx->stream));
+    if (!y_mapped)
+        CK(cudaMemcpyAsync(x_out_host, ctx->host_out, bytes, cudaMemcpyDeviceToHost, ctx->stream));
     return hb_sync(ctx);
 }
 
