@@ -792,11 +792,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
     }
-    if (ep.mode == EPI_QKV)
-        for (int c = threadIdx.x; c < a.tg; c += TC_THREADS) {
-            s_pos[c] = c < a.T ? ep.pos[c] : 0;
-            s_slot[c] = c < a.T ? ep.slot[c] : -1;
-        }
     if (warp == 1)
         tmem_alloc_pair(tmem_slot, 512);
     tc_fence_before();
@@ -953,6 +948,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const bool partial_mode = ep.mode == EPI_PARTIAL;
         float *xp = s_xp + q * 32 * TC_XP_LD;
+        if (ep.mode == EPI_QKV) {
+            // the rows' positions and slots belong to the batch plan, which the
+            // step's first kernel writes: read them after the wait for it
+            pdl_wait();
+            for (int c = et; c < a.tg; c += 128) {
+                s_pos[c] = c < a.T ? ep.pos[c] : 0;
+                s_slot[c] = c < a.T ? ep.slot[c] : -1;
+            }
+            epi_bar();
+        }
         const PairSegs seg_it(clu, a, u0, u1);
         int slot_next = 0;
         for (int seg = 0; seg < seg_it.n; ++seg) {

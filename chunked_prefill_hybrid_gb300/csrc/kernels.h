@@ -6,8 +6,13 @@
 namespace hb {
 
 // RMSNorm: y[t][i] = bf16(x[t][i] * rsqrt(mean_i x[t][i]^2 + eps) * gamma[i]).
+// meta_src / meta_dst / meta_n16: when set, the kernel also copies meta_n16
+// 16-byte words from meta_src (the batch plan in mapped, page-locked host
+// memory) to meta_dst, after its wait for the previous kernel, so that the
+// kernels after it find the plan in device memory.
 cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, int H, float eps,
-                           cudaStream_t s, bool pdl = false);
+                           cudaStream_t s, bool pdl = false, const int *meta_src = nullptr, int *meta_dst = nullptr,
+                           int meta_n16 = 0);
 
 // Reference SIMT GEMM: acc[t][n] = sum_k X[t][k] W[n][k], then the epilogue.
 // tiled: W is in the tensor-core layout [n/128][k/64][128][64], else [N][K].

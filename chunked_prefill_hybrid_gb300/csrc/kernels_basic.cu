@@ -13,10 +13,15 @@ namespace hb {
 
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) k_rmsnorm(const bf16 *__restrict__ x, const float *__restrict__ gamma,
-                                                     bf16 *__restrict__ y, int H, float eps)
+                                                     bf16 *__restrict__ y, int H, float eps,
+                                                     const uint4 *__restrict__ meta_src, uint4 *__restrict__ meta_dst,
+                                                     int meta_n16)
 {
     pdl_trigger();
     pdl_wait();
+    // every earlier kernel has finished: the plan's device copy is free to overwrite
+    for (int i = blockIdx.x * THREADS + threadIdx.x; i < meta_n16; i += gridDim.x * THREADS)
+        meta_dst[i] = meta_src[i];
     const int t = blockIdx.x;
     const bf16 *xr = x + (size_t)t * H;
     bf16 *yr = y + (size_t)t * H;
@@ -58,11 +63,14 @@ __global__ void __launch_bounds__(THREADS) k_rmsnorm(const bf16 *__restrict__ x,
 }
 
 cudaError_t launch_rmsnorm(const bf16 *x, const float *gamma, bf16 *y, int T, int H, float eps, cudaStream_t s,
-                           bool pdl)
+                           bool pdl, const int *meta_src, int *meta_dst, int meta_n16)
 {
     if (T <= 0)
         return cudaSuccess;
-    cudaError_t e = launch_kernel(pdl, k_rmsnorm<256>, dim3(T), dim3(256), 0, s, x, gamma, y, H, eps);
+    if (meta_n16 > 0 && (!meta_src || !meta_dst || ((uintptr_t)meta_src | (uintptr_t)meta_dst) % 16 != 0))
+        return cudaErrorInvalidValue;
+    cudaError_t e = launch_kernel(pdl, k_rmsnorm<256>, dim3(T), dim3(256), 0, s, x, gamma, y, H, eps,
+                                  (const uint4 *)meta_src, (uint4 *)meta_dst, meta_n16);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -332,8 +332,13 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
 
     // on the tensor-core path norm-1 of every layer but the first was
     // produced by the previous layer's final reduce
-    if (!tc || l == l_first)
-        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s, ctx->gemm_impl == 2));
+    // the step's first kernel also copies the batch plan to the device
+    if (!tc || l == l_first) {
+        const bool first = l == l_first;
+        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s, ctx->gemm_impl == 2,
+                                     first ? ctx->meta_src : nullptr, first ? ctx->d_meta : nullptr,
+                                     first ? ctx->meta_n16 : 0));
+    }
 
     EpiParams ep{};
     ep.mode = EPI_QKV;

@@ -415,7 +415,7 @@ extern "C" int hb_init(const hb_model_config *cfg, const hb_layer_weights *weigh
 
     // metadata: 3 T + 4 n_seq + block tables + attention work list
     const size_t max_seq = (size_t)c.max_decodes + HB_MAX_CHUNKS;
-    ctx->meta_cap = 3 * MT + 4 * max_seq + max_seq * c.max_blocks_per_seq + kMetaExtraWords(c);
+    ctx->meta_cap = (3 * MT + 4 * max_seq + max_seq * c.max_blocks_per_seq + kMetaExtraWords(c) + 3) / 4 * 4;
     if ((rc = ctx_alloc(ctx, (void **)&ctx->d_meta, ctx->meta_cap * sizeof(int))))
         return bail(rc);
     if (cudaMallocHost((void **)&ctx->h_err, sizeof(int)) != cudaSuccess) {
@@ -424,10 +424,13 @@ extern "C" int hb_init(const hb_model_config *cfg, const hb_layer_weights *weigh
     }
     *ctx->h_err = 0;
     for (int i = 0; i < kMetaRing; ++i) {
-        if (cudaMallocHost((void **)&ctx->h_meta[i], ctx->meta_cap * sizeof(int)) != cudaSuccess) {
+        if (cudaHostAlloc((void **)&ctx->h_meta[i], ctx->meta_cap * sizeof(int), cudaHostAllocMapped) != cudaSuccess) {
             ctx->h_meta[i] = nullptr;
             return bail(HB_ENOMEM);
         }
+        if (cudaHostGetDevicePointer((void **)&ctx->h_meta_dev[i], ctx->h_meta[i], 0) != cudaSuccess ||
+            (uintptr_t)ctx->h_meta_dev[i] % 16 != 0)
+            return bail(HB_ECUDA);
         if (cudaEventCreateWithFlags(&ctx->meta_ev[i], cudaEventDisableTiming) != cudaSuccess)
             return bail(HB_ECUDA);
     }
@@ -574,8 +577,11 @@ static int upload_plan(hb_ctx *ctx, const Plan &p, BatchDev &b)
         return rc;
     if (at > ctx->meta_cap)
         return ctx->set_error(HB_ERANGE, "metadata overflow (%zu > %zu words)", at, ctx->meta_cap);
-    CK(cudaMemcpyAsync(ctx->d_meta, hm, at * sizeof(int), cudaMemcpyHostToDevice, ctx->stream));
-    CK(cudaEventRecord(ctx->meta_ev[ctx->meta_i], ctx->stream));
+    // the step's first kernel copies the plan to d_meta (no copy breaks the
+    // chain of programmatic launches); the staging buffer is reused only
+    // after the event that launch_layers records behind the step
+    ctx->meta_src = ctx->h_meta_dev[ctx->meta_i];
+    ctx->meta_n16 = (int)((at + 3) / 4);
     return HB_OK;
 }
 
@@ -616,6 +622,8 @@ static int launch_layers(hb_ctx *ctx, const BatchDev &b, int l0, int l1, const v
         bf16 *y = (l == l1 - 1) ? (bf16 *)x_out : ((l - l0) % 2 == 0 ? ctx->xa : ctx->xb);
         if ((rc = run_layer(ctx, l, l0, l1, b, x, y)))
             return rc;
+        if (l == l0)
+            CK(cudaEventRecord(ctx->meta_ev[ctx->meta_i], ctx->stream));  // behind the plan's copy
         x = y;
     }
     return HB_OK;

@@ -78,10 +78,16 @@ struct hb_ctx {
     int *err_word = nullptr;
     int *h_err = nullptr;  // pinned: the error word read back with the stream's work
 
-    // batch metadata: pinned staging ring + one device buffer
+    // batch metadata: a ring of mapped, page-locked staging buffers + one
+    // device buffer.  A forward step's plan is copied from its staging
+    // buffer to d_meta by the step's first kernel (meta_src, meta_n16 until
+    // that launch); the KV hooks copy theirs with cudaMemcpyAsync.
     int *d_meta = nullptr;
-    size_t meta_cap = 0;
+    size_t meta_cap = 0;  // words, a multiple of 4
     int *h_meta[hb::kMetaRing] = {nullptr};
+    int *h_meta_dev[hb::kMetaRing] = {nullptr};  // the same buffers as the GPU addresses them
+    const int *meta_src = nullptr;
+    int meta_n16 = 0;
     cudaEvent_t meta_ev[hb::kMetaRing] = {nullptr};
     bool meta_used[hb::kMetaRing] = {false};
     int meta_i = 0;
