@@ -665,12 +665,13 @@ extern "C" int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const voi
     CK(cudaMemcpyAsync(ctx->host_in, x_in_host, bytes, cudaMemcpyHostToDevice, ctx->stream));
     // A page-locked output buffer that the GPU can address is written in
     // place by the last kernel's stores (every output store is a plain
-    // st.global), so no copy follows the stack; any other buffer gets the
-    // result by a device-to-host copy.
+    // st.global of 16 bytes, so the buffer must be 16-byte aligned), so no
+    // copy follows the stack; any other buffer gets the result by a
+    // device-to-host copy.
     void *y_mapped = nullptr;
     cudaPointerAttributes pa{};
     if (cudaPointerGetAttributes(&pa, x_out_host) == cudaSuccess) {
-        if (pa.type == cudaMemoryTypeHost && pa.devicePointer)
+        if (pa.type == cudaMemoryTypeHost && pa.devicePointer && (uintptr_t)pa.devicePointer % 16 == 0)
             y_mapped = pa.devicePointer;
     } else {
         cudaGetLastError();  // not a CUDA-known pointer: clear the error, copy

@@ -182,9 +182,10 @@ int hb_forward_layers(hb_ctx *ctx, const hb_batch_spec *spec, int layer_begin, i
 /* Like hb_forward, but x_in and x_out are HOST bf16 buffers: the call copies
  * x_in to the device, runs the stack and copies the result back, all on the
  * context's stream, and waits for it.  Use pinned host memory for speed:
- * a page-locked x_out_host that the GPU can address (cudaPointerGetAttributes
- * reports a device pointer for it) is written in place by the last kernel,
- * with no copy after the stack.
+ * a page-locked, 16-byte aligned x_out_host that the GPU can address
+ * (cudaPointerGetAttributes reports a device pointer for it) is written in
+ * place by the last kernel, with no copy after the stack; any other buffer
+ * is filled by a device-to-host copy.
  * The input copy starts before the batch is fully validated (it overlaps the
  * host's planning); when the batch is then rejected, the call waits for that
  * copy before it returns the error, so x_in_host is free again on return and
