@@ -597,6 +597,8 @@ static int prepare_layers(hb_ctx *ctx, const hb_batch_spec *spec, int l0, int l1
         return ctx->set_error(HB_ERANGE, "layer range [%d, %d) invalid", l0, l1);
     if (!x_in || !x_out)
         return ctx->set_error(HB_EINVAL, "x_in / x_out is NULL");
+    if (((uintptr_t)x_in | (uintptr_t)x_out) % 16 != 0)  // rows are read and written as 16-byte vectors
+        return ctx->set_error(HB_EINVAL, "x_in / x_out must be 16-byte aligned");
     for (int l = l0; l < l1; ++l)
         if (!ctx->layers[l].loaded)
             return ctx->set_error(HB_ESTATE, "layer %d has no weights", l);

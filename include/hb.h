@@ -170,7 +170,8 @@ int hb_fill_kv(hb_ctx *ctx, uint16_t bits);
 
 /* Run the batch through all layers.  x_in, x_out: device bf16 [T][hidden],
  * T = chunk_len + the further chunks' lengths + n_decodes; they may not
- * overlap.  Each layer writes the
+ * overlap and must be 16-byte aligned (HB_EINVAL otherwise, before any
+ * launch).  Each layer writes the
  * batch's new K/V into its pool at the rows' slots, then attends.  The
  * library does not advance request lengths; the scheduler does. */
 int hb_forward(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in, void *x_out);
