@@ -622,10 +622,13 @@ static int launch_layers(hb_ctx *ctx, const BatchDev &b, int l0, int l1, const v
     const bf16 *x = (const bf16 *)x_in;
     for (int l = l0; l < l1; ++l) {
         bf16 *y = (l == l1 - 1) ? (bf16 *)x_out : ((l - l0) % 2 == 0 ? ctx->xa : ctx->xb);
-        if ((rc = run_layer(ctx, l, l0, l1, b, x, y)))
+        rc = run_layer(ctx, l, l0, l1, b, x, y);
+        // behind the plan's copy; recorded on failure too, since the copying
+        // kernel may have been launched before a later launch failed
+        if (l == l0 && cudaEventRecord(ctx->meta_ev[ctx->meta_i], ctx->stream) != cudaSuccess && !rc)
+            rc = ctx->set_error(HB_ECUDA, "cudaEventRecord failed");
+        if (rc)
             return rc;
-        if (l == l0)
-            CK(cudaEventRecord(ctx->meta_ev[ctx->meta_i], ctx->stream));  // behind the plan's copy
         x = y;
     }
     return HB_OK;
