@@ -24,9 +24,10 @@
  *
  * Conventions used by every call:
  *   - Return 0 (HB_OK) or a negative HB_E* code.  On error, nothing was
- *     enqueued and hb_last_error() describes the cause.  Every argument is
- *     validated on the host before any launch, so an invalid batch never
- *     reaches the GPU.
+ *     enqueued (hb_forward_host alone may have started its input copy into
+ *     the context's own buffer, and waits for it) and hb_last_error()
+ *     describes the cause.  Every argument is validated on the host before
+ *     any launch, so an invalid batch never reaches the GPU.
  *   - "device" pointers are CUDA device memory of the context's GPU; "host"
  *     pointers are read only during the call.
  *   - bf16 tensors are raw 16-bit patterns, row-major, densely packed.
