@@ -286,6 +286,34 @@ def time_steps(torch, ctx, fn, steps, world):
     return e0.elapsed_time(e1)
 
 
+def profiled(torch, ctx, fn, steps, world):
+    """Per-kind (total ms, launches) over `steps` calls of fn, from the
+    library's CUDA events around every launch."""
+    ctx.profile(True)
+    time_steps(torch, ctx, fn, steps, world)
+    ctx.sync()
+    prof = ctx.profile_read()
+    ctx.profile(False)
+    return prof
+
+
+GEMM_KINDS = ("gemm_qkv", "gemm_o", "gemm_gate_up", "gemm_down")
+
+
+def gemm_decode_cost(prof_hybrid, prof_chunk, prof_decode, steps, D):
+    """Per-decode-token cost on the linear ops alone: the GEMM launches of
+    each batch (each with its reduce pass), marginal over the chunk alone,
+    (hybrid - chunk alone) / D, against decode-only / D.  The profiled times
+    come from events around every launch, so each batch's sum leaves out the
+    overlap of neighbouring launches in the same way."""
+    def gemm_ms(prof):
+        return sum(prof.get(k, (0.0, 0))[0] for k in GEMM_KINDS) / steps
+    gh, gc, gd = gemm_ms(prof_hybrid), gemm_ms(prof_chunk), gemm_ms(prof_decode)
+    marginal = (gh - gc) / D
+    return {"ms_gemm_hybrid": gh, "ms_gemm_chunk_alone": gc, "ms_gemm_decode_only": gd,
+            "per_decode_cost_ratio": (gd / D) / marginal if marginal > 0 else None}
+
+
 # ncu summaries under profiles/ that carry a measured DRAM traffic figure for
 # a kernel: "traffic_bytes_per_launch: N" and "sources: a b c" (files under
 # the package's csrc/) with "sources_sha256: H" of their concatenated bytes.
@@ -627,6 +655,14 @@ def main():
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     e2e = {"value": world * T * args.steps / e2e_s, "unit": "tokens/s",
            "h2d_bytes_per_step": T * dims.hidden * 2, "d2h_bytes_per_step": T * dims.hidden * 2}
+
+    # 5) the per-decode cost on GEMM time alone (an extra figure: the line stays valid without it)
+    try:
+        prof_chunk = profiled(torch, ctx, lambda: ctx.forward(chunk_alone, x_chk, y_chk), args.steps, world)
+        prof_dec = profiled(torch, ctx, lambda: ctx.forward(dec_only, x_dec, y_dec), args.steps, world)
+        decode["gemm_time"] = gemm_decode_cost(prof, prof_chunk, prof_dec, args.steps, D)
+    except Exception as e:  # noqa: BLE001
+        decode["gemm_time"] = {"error": str(e)[:200]}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -61,3 +61,21 @@ def test_committed_profiles_parse():
     for kind in bench.TRAFFIC_PROFILES:
         v = bench.measured_traffic(kind)
         assert v is None or v > 1e6
+
+
+def test_gemm_decode_cost_uses_the_linear_ops_only():
+    steps, D = 10, 18
+    # per-kind (total ms over the steps, launches); attention and norms must not count
+    hybrid = {"gemm_qkv": (0.50, 10), "gemm_o": (0.40, 10), "gemm_gate_up": (0.90, 10), "gemm_down": (0.50, 10),
+              "attention": (1.0, 10), "rmsnorm": (0.1, 10)}
+    chunk = {"gemm_qkv": (0.48, 10), "gemm_o": (0.38, 10), "gemm_gate_up": (0.86, 10), "gemm_down": (0.48, 10),
+             "attention": (0.5, 10)}
+    dec = {"gemm_qkv": (0.45, 10), "gemm_o": (0.35, 10), "gemm_gate_up": (0.80, 10), "gemm_down": (0.45, 10),
+           "attention": (0.6, 10)}
+    r = bench.gemm_decode_cost(hybrid, chunk, dec, steps, D)
+    assert r["ms_gemm_hybrid"] == pytest.approx(0.23)
+    assert r["ms_gemm_chunk_alone"] == pytest.approx(0.22)
+    assert r["ms_gemm_decode_only"] == pytest.approx(0.205)
+    assert r["per_decode_cost_ratio"] == pytest.approx((0.205 / D) / ((0.23 - 0.22) / D))
+    # no marginal cost measured: no ratio
+    assert bench.gemm_decode_cost(chunk, chunk, dec, steps, D)["per_decode_cost_ratio"] is None
