@@ -4,40 +4,21 @@
 // the chunk's rows and the piggybacked decode rows together (SARATHI summary,
 // section 3.4 "Decode-Maximal Batching", "How fusion works").
 //
-// Orientation ("swap AB"): the MMA's M is 128 weight rows (output features)
-// and its N is a group of the batch's tokens, a multiple of 16 up to 256.  A
-// batch of T rows is cut into G = ceil(T / 256) equal token groups, so
-// T = 256 + 18 = 274 runs as 2 x 144 columns (5% padding) instead of three
-// 128-row tiles (29%) -- the tile-quantization effect of SARATHI summary
-// section 3.4 / Figure 7 is kept small by sizing the token tile to T.
-//
-// The G CTAs that handle the G token groups of one weight tile form a
-// thread-block cluster: each fetches a slice of the weight tile and
-// multicasts it to all of them, so every weight byte still leaves HBM once.
+// Orientation ("swap AB"): the MMA's M is weight rows (output features) and
+// its N is the batch's tokens, a multiple of 16 up to 256 per MMA, so a batch
+// of T rows is padded to 16 rather than to a 128-row tile -- the
+// tile-quantization effect of SARATHI summary section 3.4 / Figure 7 is kept
+// small by sizing the token tile to T.
 //
 // Weights are stored tiled, [n_tile][k_block][128][64], so every TMA box is
-// a contiguous run of HBM and each cluster streams a contiguous range.
+// a contiguous 16 KB run of HBM and each CTA streams a contiguous range.
 //
-// Work split ("stream-K"): the (weight tile, k-block) units are divided
-// evenly over a persistent grid of clusters, one CTA per SM.  A tile whose
-// k-range spans several clusters is finished either by the last CTA to
-// arrive (per-tile arrival counter, no waiting), which sums every
-// contributor's fp32 partial in cluster order -- a fixed order, so results
-// do not depend on timing -- or, in partial mode, by a separate kernel.
-//
-//   warp 0      TMA producer: W slice (multicast) and this CTA's X tokens
-//   warp 1      TMEM owner; one thread issues tcgen05.mma (M=128, N=n_sub,
-//               K=16, 4 per k-block) into one of two TMEM accumulators
-//   warps 2..5  epilogue: tcgen05.ld (one TMEM lane = one output feature,
-//               columns = tokens), transposed through shared memory, fused
-//               epilogue on (token, 16 features) with 16-byte accesses
+// The kernel (k_gemm_pair, further down) runs on CTA pairs with the 2-SM
+// MMA, data-parallel, stream-K or one data-parallel wave plus a stream-K
+// tail; its own comment describes it.  Stream-K tiles leave fp32 partials
+// summed in a fixed contributor order, so results do not depend on timing.
 // Every mbarrier wait is bounded (wall clock); on a timeout the kernel
 // records an error in the device error word, drains and frees TMEM.
-//
-// That is k_gemm_tc, the token-group kernel.  The default is k_gemm_pair
-// further down: the same product on CTA pairs with the 2-SM MMA, data-
-// parallel, stream-K or one data-parallel wave plus a stream-K tail; its own
-// comment describes it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -55,7 +36,6 @@ constexpr int TC_BK = 64;
 constexpr int TC_THREADS = 192;
 constexpr int TC_W_BYTES = TC_BM * TC_BK * 2;
 constexpr uint64_t TC_WAIT_NS = 2000000000ull;  // 2 s
-constexpr int TC_MAX_G = 8;
 
 struct TcArgs {
     int T, N, K;
@@ -66,7 +46,6 @@ struct TcArgs {
     int tg;
     int n_sub32;      // n_sub rounded up to 32 (the epilogue's column chunks)
     int nslot;        // pair kernel: TMEM accumulator slots of n_sub columns
-    int wpiece;       // weight-tile rows each CTA fetches and multicasts
     int units, grid;  // units = n_mtiles * nkb over `grid` clusters
     int stages, slots;
     float *ws;        // [grid * G][slots][tg][128]
@@ -151,12 +130,6 @@ constexpr int TC_MAX_TG = 512;
 constexpr int TC_META_BYTES = 2 * TC_MAX_TG * 4;
 constexpr int TC_XP_LD = 33;
 constexpr int TC_XP_BYTES = 4 * 32 * TC_XP_LD * 4;
-
-__host__ __device__ inline int tc_stage_bytes(int tg) { return TC_W_BYTES + tg * TC_BK * 2; }
-__host__ __device__ inline int tc_smem_bytes(int tg, int stages)
-{
-    return stages * tc_stage_bytes(tg) + 256 + TC_META_BYTES + TC_XP_BYTES + 1024;
-}
 
 __device__ __forceinline__ int unit_owner(long long u, const TcArgs &a)
 {
@@ -274,314 +247,6 @@ __device__ __forceinline__ void fixup_tile(const EpiParams &ep, const TcArgs &a,
         for (int j = 0; j < 32; ++j)
             r[j] = __float_as_uint(acc[j]);
         emit_cols(ep, s_pos, s_slot, xp, t_base, c0, ncol, nb, lane, r);
-    }
-}
-
-__global__ void __launch_bounds__(TC_THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
-              EpiParams ep)
-{
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int S = a.stages;
-    const int stage_bytes = tc_stage_bytes(a.tg);
-    uint64_t *full = (uint64_t *)(smem + (size_t)S * stage_bytes);
-    uint64_t *empty = full + S;  // one per group of `rel` consecutive stages
-    uint64_t *accf = empty + S;  // [2]
-    uint64_t *acce = accf + 2;   // [2]
-    uint64_t *drain = acce + 2;
-    uint32_t *tmem_slot = (uint32_t *)(drain + 1);
-    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
-    volatile int *last_flag = abort_flag + 1;
-    int *s_pos = (int *)(smem + (size_t)S * stage_bytes + 256);  // [TC_MAX_TG]
-    int *s_slot = s_pos + TC_MAX_TG;                               // [TC_MAX_TG]
-    float *s_xp = (float *)(s_slot + TC_MAX_TG);                   // [4][32][TC_XP_LD]
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = a.G > 1 ? (int)cluster_ctarank() : 0;  // token group of this CTA
-    const int clu = blockIdx.x / a.G;                        // cluster: the unit owner
-    const int cta = clu * a.G + rank;                        // workspace index
-    const uint16_t mask = (uint16_t)((1u << a.G) - 1u);
-    const int u0 = unit_begin(clu, a), u1 = unit_begin(clu + 1, a);
-    const int t_base = rank * a.tg;
-    const int n_acc = a.nsub == 1 ? 2 : 1;  // accumulator buffers
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s)
-            mbar_init(&full[s], 1);
-        for (int s = 0; s < S / a.rel; ++s)
-            mbar_init(&empty[s], a.G);  // released by the MMA of every CTA of the cluster
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&accf[b], 1);
-            mbar_init(&acce[b], 4);  // one arrival per epilogue warp
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmW);
-        tma_prefetch_desc(&tmX);
-    }
-    if (ep.mode == EPI_QKV)
-        for (int c = threadIdx.x; c < a.tg; c += TC_THREADS) {
-            const int t = t_base + c;
-            s_pos[c] = t < a.T ? ep.pos[t] : 0;
-            s_slot[c] = t < a.T ? ep.slot[t] : -1;
-        }
-    if (warp == 1)
-        tmem_alloc(tmem_slot, 512);  // two accumulators at columns 0 and 256
-    tc_fence_before();
-    __syncthreads();
-    if (a.G > 1)
-        cluster_sync();  // peers' barriers are initialised before any multicast lands
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    // Ring position: stage s of S, lap parity ph; stages are released in
-    // groups of rel (1 or 2) consecutive stages.  Kept as counters so the
-    // single-warp loops below do no integer division.
-    const int rel_mask = a.rel - 1, rel_shift = a.rel == 2 ? 1 : 0;
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        // The whole warp runs this loop (warp-uniform values); one elected
-        // lane issues each copy.
-        // W: rows [w0, w0 + wpiece) of the stage's weight tile, multicast
-        // to the cluster (slices may overlap at the end: the overlapping
-        // rows carry identical data and are counted in the expected bytes).
-        // X: this CTA's own token rows, nsub boxes of n_sub.
-        const uint32_t bytes = (uint32_t)(a.G * a.wpiece * TC_BK * 2 + a.tg * TC_BK * 2);
-        const int w0 = min(rank * a.wpiece, TC_BM - a.wpiece);
-        const SegIter seg_it(u0, u1, a.nkb);
-        int it = 0, s = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int i = 0; i < seg_it.n && ok; ++i) {
-            int sa, sb;
-            seg_it.get(i, sa, sb);
-            if (rank == 0)
-                for (int u = sa; u < min(sb, sa + TC_PREFETCH); ++u)
-                    bulk_prefetch_l2_elect(a.w_tiled + (size_t)u * TC_BM * TC_BK, TC_W_BYTES);
-            const int mt = sa / a.nkb;  // a segment lies within one weight tile
-            int w_row = sa * TC_BM + w0;  // row of the tiled weights: (mt * nkb + kb) * 128 + w0
-            int kx = (sa - mt * a.nkb) * TC_BK;
-            for (int u = sa; u < sb; ++u, ++it, w_row += TC_BM, kx += TC_BK) {
-                if (rank == 0 && u + TC_PREFETCH < sb)
-                    bulk_prefetch_l2_elect(a.w_tiled + (size_t)(u + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES);
-                if (it >= S && (s & rel_mask) == 0 &&
-                    !__all_sync(0xffffffffu, mbar_wait(&empty[s >> rel_shift], ph ^ 1u, abort_flag, TC_WAIT_NS))) {
-                    if (lane == 0) {
-                        set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    ok = false;
-                    break;
-                }
-                uint8_t *sw = smem + (size_t)s * stage_bytes;
-                mbar_expect_tx_elect(&full[s], bytes);
-                if (a.G > 1)
-                    tma_load_2d_multicast_elect(sw + w0 * TC_BK * 2, &tmW, &full[s], 0, w_row, mask);
-                else
-                    tma_load_2d_elect(sw, &tmW, &full[s], 0, w_row);
-#pragma unroll
-                for (int sub = 0; sub < 2; ++sub)
-                    if (sub < a.nsub)
-                        tma_load_2d_elect(sw + TC_W_BYTES + sub * a.n_sub * TC_BK * 2, &tmX, &full[s], kx,
-                                          t_base + sub * a.n_sub);
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-        // tail: wait until every CTA of the cluster released the last use of
-        // each stage pair, so no arrival or multicast write is still in
-        // flight to this CTA's shared memory when it exits
-        for (int k = (it > S ? it - S : 0); k < it; ++k)
-            if (k % S % a.rel == 0)
-                mbar_wait(&empty[(k % S) / a.rel], (uint32_t)(k / S) & 1u, ok ? abort_flag : nullptr,
-                          ok ? TC_WAIT_NS : TC_WAIT_NS / 4);
-        if (!ok) {
-            for (int k = (it > S ? it - S : 0); k < it; ++k)
-                mbar_wait(&full[k % S], (uint32_t)(k / S) & 1u, nullptr, TC_WAIT_NS / 4);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop; one elected lane issues each MMA
-        // and commit.  A commit costs about as much as four short MMAs, so
-        // for N < 224 stages are released in pairs (one commit per two
-        // k-blocks).
-        const uint32_t idesc = idesc_bf16_f32(TC_BM, a.n_sub);
-        // descriptors of stage 0; a stage, a K step (32 bytes) and an MMA's
-        // token block only move the start-address field (address >> 4)
-        const uint64_t desc0 = sdesc_kmajor_sw128(smem_u32(smem));
-        const uint32_t stage16 = (uint32_t)stage_bytes >> 4;
-        const uint32_t xsub16 = (uint32_t)(a.n_sub * TC_BK * 2) >> 4;
-        const SegIter seg_it(u0, u1, a.nkb);
-        int s = 0;
-        uint32_t ph = 0, st16 = 0;
-        bool ok = true;
-        for (int seg = 0; seg < seg_it.n && ok; ++seg) {
-            int sa, sb;
-            seg_it.get(seg, sa, sb);
-            const int buf = seg % n_acc;
-            const int use = seg / n_acc;
-            if (use > 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(&acce[buf], (uint32_t)(use - 1) & 1u, abort_flag, TC_WAIT_NS))) {
-                if (lane == 0) {
-                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d0 = tmem + (uint32_t)(buf * 256);
-            for (int u = sa; u < sb; ++u) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, TC_WAIT_NS))) {
-                    if (lane == 0) {
-                        set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t dw = desc0 + st16;
-                const uint64_t dx = dw + (TC_W_BYTES >> 4);
-#pragma unroll
-                for (int sub = 0; sub < 2; ++sub) {
-                    if (sub < a.nsub) {
-#pragma unroll
-                        for (int k = 0; k < TC_BK / 16; ++k)
-                            mma_bf16_elect(d0 + (uint32_t)(sub * 256), dw + (uint32_t)(k * 2),
-                                           dx + (uint32_t)(sub * xsub16 + k * 2), idesc,
-                                           (u > sa || k > 0) ? 1u : 0u);
-                    }
-                }
-                if ((s & rel_mask) == rel_mask) {
-                    if (a.G > 1)
-                        mma_commit_multicast_elect(&empty[s >> rel_shift], mask);
-                    else
-                        mma_commit_elect(&empty[s >> rel_shift]);
-                }
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                    st16 = 0;
-                } else {
-                    st16 += stage16;
-                }
-            }
-            if (!ok)
-                break;
-            mma_commit_elect(&accf[buf]);
-        }
-        if (ok && (s & rel_mask) != 0) {
-            // release the partly used last group
-            if (a.G > 1)
-                mma_commit_multicast_elect(&empty[(s - 1) >> rel_shift], mask);
-            else
-                mma_commit_elect(&empty[(s - 1) >> rel_shift]);
-        }
-        if (!ok) {
-            mma_commit_elect(drain);
-            mbar_wait(drain, 0, nullptr, TC_WAIT_NS / 4);
-        }
-    } else if (warp >= 2) {
-        // ------------------------------------------------------ epilogue
-        // With the 32x32b TMEM load a lane holds one output feature (TMEM
-        // lane) and its registers hold consecutive token columns, so a warp
-        // owns 32 consecutive features of each token: plain warp-wide stores
-        // are coalesced and no shared-memory transpose is needed.  The four
-        // warps work independently on their quadrants of the 128 features.
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        const int et = threadIdx.x - 64;
-        const int f = q * 32 + lane;  // feature within the weight tile
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const bool partial_mode = ep.mode == EPI_PARTIAL;
-        const SegIter seg_it(u0, u1, a.nkb);
-        for (int seg = 0; seg < seg_it.n; ++seg) {
-            int sa, sb;
-            seg_it.get(seg, sa, sb);
-            const int mt = sa / a.nkb, kb0 = sa % a.nkb;
-            const int kb1 = kb0 + (sb - sa);
-            const int tile = mt * a.G + rank;  // arrival counter of this CTA's tile
-            const int buf = seg % n_acc;
-            const int use = seg / n_acc;
-            const bool whole = (kb0 == 0 && kb1 == a.nkb);
-            const bool direct = whole && !partial_mode;
-            const int nb = mt * TC_BM + q * 32;  // first feature of this warp
-            if (direct && ep.mode == EPI_RESID) {
-                // bring this warp's residual rows into L2 while the MMAs run
-                for (int c = lane; c < a.tg; c += 32) {
-                    const int t = t_base + c;
-                    if (t < a.T && nb < a.N)
-                        prefetch_l2(ep.resid + (size_t)t * a.N + nb);
-                }
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait(&accf[buf], (uint32_t)use & 1u, abort_flag, TC_WAIT_NS * 2))) {
-                if (lane == 0 && !*abort_flag) {
-                    set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                break;
-            }
-            tc_fence_after();
-            const uint32_t d0 = tmem + lane_base + (uint32_t)(buf * 256);
-            const int slot = mt - u0 / a.nkb;
-            float *ws_mine = a.ws + ((size_t)cta * a.slots + slot) * a.tg * TC_BM;
-            for (int sub = 0; sub < a.nsub; ++sub) {
-                for (int c0 = 0; c0 < a.n_sub; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0), *reinterpret_cast<uint32_t(*)[16]>(r));
-                    tmem_ld_32x32b_x16(d0 + (uint32_t)(sub * 256 + c0 + 16),
-                                       *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-                    tmem_ld_wait();
-                    const int col0 = sub * a.n_sub + c0;  // token column of r[0] in this CTA
-                    const int ncol = min(32, a.n_sub - c0);
-                    if (direct) {
-                        emit_cols(ep, s_pos, s_slot, s_xp + q * 32 * TC_XP_LD, t_base, col0, ncol, nb, lane, r);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (j < ncol)
-                                ws_mine[(size_t)(col0 + j) * TC_BM + f] = __uint_as_float(r[j]);
-                    }
-                }
-            }
-            // accumulator buffer free for the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&acce[buf]);
-            if (!whole && !partial_mode) {
-                // stream-K fixup: the last contributor to arrive finishes the tile
-                __threadfence();
-                epi_bar();
-                const int c_lo = unit_owner((long long)mt * a.nkb, a);
-                const int c_hi = unit_owner((long long)mt * a.nkb + a.nkb - 1, a);
-                if (et == 0) {
-                    const int old = atomicAdd(&a.counters[tile], 1);
-                    *last_flag = (old == c_hi - c_lo);
-                }
-                epi_bar();
-                if (*last_flag) {
-                    __threadfence();
-                    fixup_tile(ep, a, s_pos, s_slot, s_xp + q * 32 * TC_XP_LD, rank, t_base, mt, c_lo, c_hi, nb, f,
-                               lane);
-                    if (et == 0)
-                        a.counters[tile] = 0;
-                }
-                epi_bar();
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (a.G > 1)
-        cluster_sync();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -1133,13 +798,6 @@ bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, in
     return encode_2d(m, tiled, TC_BK, npad * nkb, TC_BK * 2, TC_BK, (uint32_t)box_rows);
 }
 
-int tc_weight_box_rows(int T)
-{
-    const int G = tc_shape(T).G;
-    const int piece = ((TC_BM + G - 1) / G + 7) / 8 * 8;
-    return G > 1 ? piece : TC_BM;
-}
-
 // The paged K or V pool [num_blocks][n_kv][16][d] as a 2D tensor of
 // num_blocks * n_kv * 16 rows of d elements, in boxes of 16 rows x 64
 // elements (128-byte swizzle): one box is half (d = 128) or all (d = 64) of
@@ -1147,20 +805,6 @@ int tc_weight_box_rows(int T)
 bool make_tmap_kv_pool(CUtensorMap *m, const void *pool, int num_blocks, int n_kv, int d)
 {
     return encode_2d(m, pool, (uint64_t)d, (uint64_t)num_blocks * n_kv * 16, (uint64_t)d * 2, 64, 16);
-}
-
-// G = ceil(T / 256) equal token groups of n_sub (a multiple of 16) columns,
-// one MMA of N = n_sub per k-block and two TMEM accumulators per CTA, so
-// the epilogue of one tile overlaps the main loop of the next.  (The kernel
-// also takes two MMAs per k-block, nsub = 2, into one accumulator pair.)
-TcShape tc_shape(int T)
-{
-    TcShape sh;
-    sh.G = (T + 255) / 256;
-    sh.nsub = 1;
-    sh.n_sub = ((T + sh.G - 1) / sh.G + 15) / 16 * 16;
-    sh.tg = sh.nsub * sh.n_sub;
-    return sh;
 }
 
 // Slots (partial tiles) a CTA can hold: the most tiles any cluster's unit range touches.
@@ -1174,119 +818,6 @@ static int tc_grid(long long units, int max_clusters)
 {
     return (int)(units < max_clusters ? units : max_clusters);
 }
-
-size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes)
-{
-    size_t need = 0;
-    for (int i = 0; i < n_shapes; ++i)
-        for (int T = 1; T <= max_tokens && T <= 2048; ++T) {
-            const TcShape sh = tc_shape(T);
-            const int n_mtiles = (Ns[i] + TC_BM - 1) / TC_BM;
-            const int nkb = (Ks[i] + TC_BK - 1) / TC_BK;
-            const long long units = (long long)n_mtiles * nkb;
-            const int grid = tc_grid(units, num_sms / sh.G);
-            const size_t n = (size_t)grid * sh.G * tc_slots(units, grid, nkb) * sh.tg * TC_BM;
-            if (n > need)
-                need = n;
-        }
-    return need;
-}
-
-cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
-                           const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part)
-{
-    if (T <= 0)
-        return cudaSuccess;
-    if (K % 8 != 0)
-        return cudaErrorInvalidValue;
-    const TcShape sh = tc_shape(T);
-    if (sh.G > TC_MAX_G)
-        return cudaErrorInvalidValue;
-    TcArgs a = {};
-    a.T = T;
-    a.N = N;
-    a.K = K;
-    a.n_mtiles = (N + TC_BM - 1) / TC_BM;
-    a.nkb = (K + TC_BK - 1) / TC_BK;
-    a.G = sh.G;
-    a.nsub = sh.nsub;
-    a.n_sub = sh.n_sub;
-    a.tg = sh.tg;
-    a.n_sub32 = (sh.n_sub + 31) / 32 * 32;
-    {
-        int piece = (TC_BM + a.G - 1) / a.G;
-        piece = (piece + 7) / 8 * 8;  // whole 1 KB swizzle atoms
-        a.wpiece = piece;
-    }
-    const long long units = (long long)a.n_mtiles * a.nkb;
-    if (units > (1ll << 30) || (long long)a.n_mtiles * a.G > rt.n_counters)
-        return cudaErrorInvalidValue;
-    a.units = (int)units;
-    int stages = 10;
-    while (stages > 2 && tc_smem_bytes(a.tg, stages) > rt.max_smem)
-        stages -= 2;  // even: stages are released in pairs
-    if (tc_smem_bytes(a.tg, stages) > rt.max_smem)
-        return cudaErrorInvalidConfiguration;
-    a.stages = stages;
-    const int smem = tc_smem_bytes(a.tg, stages);
-    static int configured = 0;
-    if (configured < rt.max_smem) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, rt.max_smem);
-        if (e != cudaSuccess)
-            return e;
-        configured = rt.max_smem;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.G;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // clusters that can be resident at once, cached per (cluster size, stages)
-    static int max_clusters[TC_MAX_G + 1][11] = {};
-    int &mc = max_clusters[a.G][stages];
-    if (!mc) {
-        cfg.gridDim = dim3((unsigned)(rt.num_sms / a.G * a.G));
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc, &cfg) != cudaSuccess || n <= 0) {
-            cudaGetLastError();
-            n = rt.num_sms / a.G;
-        }
-        mc = n < rt.num_sms / a.G ? n : rt.num_sms / a.G;
-    }
-    a.grid = tc_grid(units, mc);
-    a.slots = tc_slots(units, a.grid, a.nkb);
-    if ((size_t)a.grid * a.G * a.slots * a.tg * TC_BM > rt.ws_floats)
-        return cudaErrorInvalidValue;
-    if (part) {
-        part->ws = rt.ws;
-        part->grid = a.grid;
-        part->G = a.G;
-        part->units = a.units;
-        part->nkb = a.nkb;
-        part->tg = a.tg;
-        part->slots = a.slots;
-        part->pair = 0;
-    }
-    a.ws = rt.ws;
-    a.counters = rt.counters;
-    a.w_tiled = W_tiled;
-    a.rel = (a.tg < 224) ? 2 : 1;  // 1 or 2: the kernel's ring counters assume a power of two <= 2
-    CUtensorMap tmX;
-    if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)a.n_sub))
-        return cudaErrorInvalidValue;
-    cfg.gridDim = dim3((unsigned)(a.grid * a.G));
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, tmW, tmX, a, ep);
-    if (e != cudaSuccess)
-        return e;
-    return cudaGetLastError();
-}
-
 
 // ---------------------------------------------------------- pair launcher
 TcShape tc_pair_shape(int T)
@@ -1368,7 +899,6 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
     a.nslot = pair_nslot(sh.n_sub);
     if (a.nslot < a.nsub || a.tg > TC_MAX_TG)
         return cudaErrorInvalidValue;
-    a.wpiece = TC_BM;
     const int n_mpairs = (a.n_mtiles + 1) / 2;
     if (dp_tiles < 0 || dp_tiles >= n_mpairs || (dp_tiles > 0 && (ep.mode == EPI_PARTIAL || !part)) ||
         (dp_tiles > 0 && (long long)(n_mpairs - dp_tiles) * a.nkb < dp_tiles))

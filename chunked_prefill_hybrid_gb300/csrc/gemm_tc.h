@@ -7,12 +7,11 @@
 
 namespace hb {
 
-// Token tiling of a batch of T rows: G groups (one per CTA of a cluster) of
-// tg = nsub * n_sub columns, nsub MMAs of N = n_sub (<= 256) per k-block.
+// Token tiling of a batch of T rows on a CTA pair (G = 2): tg = nsub * n_sub
+// columns, nsub MMAs of N = n_sub (<= 256) per k-block.
 struct TcShape {
     int G, nsub, n_sub, tg;
 };
-TcShape tc_shape(int T);
 
 // Device resources the GEMM needs (owned by the context).
 struct TcRuntime {
@@ -23,40 +22,27 @@ struct TcRuntime {
     int n_counters = 0;
 };
 
-// Where each CTA of one launch left its fp32 partial tiles.  Weight tile mt
-// covers units [mt*nkb, mt*nkb+nkb) of an even split of `units` over `grid`
-// clusters of G CTAs; CTA rank r of a cluster holds token group r (tokens
-// r*tg ..).  Cluster c's rank-r CTA keeps its share of tile mt at slot
-// (mt - first tile of c), element [col][feature % 128] of
-// ws + (((c * G + r) * slots + slot) * tg) * 128.
-// Pair kernel (pair = 1): units are (weight-tile pair, k-block) over `grid`
-// CTA pairs; CTA r of pair c holds weight tile 2p + r for all T tokens
-// (col = token) at slot (p - first tile pair of c) of
-// ws + (((c * 2 + r) * slots + slot) * tg) * 128.
+// Where each CTA of one launch left its fp32 partial tiles.  Units are
+// (weight-tile pair, k-block), split evenly over `grid` CTA pairs; tile pair
+// p covers units [p*nkb, p*nkb+nkb).  CTA r of pair c holds weight tile
+// 2p + r for all T tokens (col = token) at slot (p - first tile pair of c),
+// element [col][feature % 128] of ws + (((c * G + r) * slots + slot) * tg) * 128
+// with G = 2.
 struct TcPartition {
     const float *ws = nullptr;
-    int grid = 0, G = 1, units = 0, nkb = 0, tg = 0, slots = 0;
-    int pair = 0;
+    int grid = 0, G = 2, units = 0, nkb = 0, tg = 0, slots = 0;
+    int pair = 1;
 };
 
-// Unit row (tile or tile pair), CTA rank and token column holding the
-// partials of output (t, feature tile mt) in a partition.
+// Unit row (tile pair), CTA rank and token column holding the partials of
+// output (t, feature tile mt) in a partition.
 __host__ __device__ inline void tc_part_loc(const TcPartition &p, int t, int mt, int &urow, int &r, int &col)
 {
-    if (p.pair) {
-        urow = mt >> 1;
-        r = mt & 1;
-        col = t;
-    } else {
-        urow = mt;
-        r = t / p.tg;
-        col = t % p.tg;
-    }
+    (void)p;
+    urow = mt >> 1;
+    r = mt & 1;
+    col = t;
 }
-
-// Workspace floats needed for any batch of up to max_tokens rows and the
-// given (N, K) shapes.
-size_t tc_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes);
 
 // Weights in the tiled layout [n_tile][k_block][128][64] (zero padded).
 size_t tiled_weight_elems(int N, int K);
@@ -65,9 +51,8 @@ size_t tiled_weight_elems(int N, int K);
 cudaError_t launch_tile_weights(const bf16 *src, bf16 *dst, int N, int K, int mode, int a, cudaStream_t s);
 // The paged K or V pool as a TMA map of 16-row x 64-element boxes.
 bool make_tmap_kv_pool(CUtensorMap *m, const void *pool, int num_blocks, int n_kv, int d);
-// box_rows: 128, or the multicast slice of tc_weight_box_rows(T).
+// The tiled weights as a TMA map of boxes of box_rows (128) x 64 elements.
 bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, int box_rows);
-int tc_weight_box_rows(int T);
 
 // Largest batch one pair-kernel launch takes (callers cut larger ones).
 constexpr int TC_PAIR_MAX_T = 512;
@@ -96,12 +81,6 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
 // pairs than the GPU has CTA pairs and the rest gives every pair at least one
 // k-block; else 0.
 int tc_pair_dp_tiles(const TcRuntime &rt, int N, int K);
-
-// acc[t][n] = sum_k X[t][k] W[n][k] on the tensor cores, then the epilogue.
-// tmW: map of the tiled W; X: device [T][K] bf16 (K % 8 == 0).
-// W_tiled: the tiled weights tmW describes (streamed into L2 ahead of use).
-cudaError_t launch_gemm_tc(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
-                           const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr);
 
 // out = bf16(resid + sum of the partial tiles of `part`) for T x N outputs;
 // if gamma: norm_out = bf16(out * rsqrt(mean(out^2) + eps) * gamma) per row.

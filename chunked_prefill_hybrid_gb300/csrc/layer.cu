@@ -13,21 +13,10 @@ using namespace hb;
 
 namespace hb {
 
-// Tensor maps of a layer's four tiled weights, one per weight-slice height
-// (the slice each CTA of a cluster multicasts depends on the batch's token
-// groups, see tc_weight_box_rows).
-constexpr int kBoxRows[6] = {128, 64, 48, 32, 24, 16};
+// Tensor maps of a layer's four tiled weights (128-row boxes).
 enum WKind { W_QKV = 0, W_O, W_GU, W_D };
 struct LayerMaps {
-    CUtensorMap m[4][6];
-    const CUtensorMap &get(int kind, int T) const
-    {
-        const int rows = tc_weight_box_rows(T);
-        int i = 0;
-        while (i < 5 && kBoxRows[i] != rows)
-            ++i;
-        return m[kind][i];
-    }
+    CUtensorMap m[4];
 };
 
 struct FastPath {
@@ -67,10 +56,7 @@ int hb_init_fast_path(hb_ctx *ctx)
         const hb_model_config &c = ctx->cfg;
         const int Ns[4] = {ctx->n_qkv, c.hidden, ctx->n_gu, c.hidden};
         const int Ks[4] = {c.hidden, c.n_heads * c.head_dim, c.hidden, c.ffn};
-        rt.ws_floats = tc_workspace_floats(ctx->num_sms, c.max_tokens, Ns, Ks, 4);
-        const size_t pair_floats = tc_pair_workspace_floats(ctx->num_sms, c.max_tokens, Ns, Ks, 4);
-        if (rt.ws_floats < pair_floats)
-            rt.ws_floats = pair_floats;
+        rt.ws_floats = tc_pair_workspace_floats(ctx->num_sms, c.max_tokens, Ns, Ks, 4);
         const size_t floor_floats = (size_t)ctx->num_sms * 2 * 512 * 128;  // room for hb_gemm_test shapes
         if (rt.ws_floats < floor_floats)
             rt.ws_floats = floor_floats;
@@ -102,13 +88,11 @@ int hb_init_fast_path(hb_ctx *ctx)
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerDev &L = ctx->layers[l];
         LayerMaps &m = f->maps[l];
-        for (int i = 0; i < 6; ++i) {
-            if (!make_tmap_tiled_weights(&m.m[W_QKV][i], L.w_qkv, ctx->n_qkv, H, kBoxRows[i]) ||
-                !make_tmap_tiled_weights(&m.m[W_O][i], L.w_o, H, qd, kBoxRows[i]) ||
-                !make_tmap_tiled_weights(&m.m[W_GU][i], L.w_gu, ctx->n_gu, H, kBoxRows[i]) ||
-                !make_tmap_tiled_weights(&m.m[W_D][i], L.w_d, H, c.ffn, kBoxRows[i]))
-                return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
-        }
+        if (!make_tmap_tiled_weights(&m.m[W_QKV], L.w_qkv, ctx->n_qkv, H, 128) ||
+            !make_tmap_tiled_weights(&m.m[W_O], L.w_o, H, qd, 128) ||
+            !make_tmap_tiled_weights(&m.m[W_GU], L.w_gu, ctx->n_gu, H, 128) ||
+            !make_tmap_tiled_weights(&m.m[W_D], L.w_d, H, c.ffn, 128))
+            return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable?)");
     }
     f->kv_maps.resize(2 * (size_t)c.n_layers);
     for (int l = 0; l < c.n_layers; ++l)
@@ -164,25 +148,21 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
             return ctx->set_error(HB_ECUDA, "launch %s failed: %s", kKindNames[kind], cudaGetErrorString(e_)); \
     } while (0)
 
-// Largest token slab of one tensor-core GEMM launch (8 token groups of 256).
-constexpr int kSlab = 2048;  // rows per launch of the token-group kernel
-// rows per launch of the selected tensor-core kernel for a batch of T rows:
-// the fewest launches, with their rows balanced (each launch streams the
-// weights once, so 513 rows run as 257 + 256 rather than 512 + 1)
-static int slab_rows(const hb_ctx *ctx, int T)
+// rows per launch of the tensor-core kernel for a batch of T rows: the
+// fewest launches, with their rows balanced (each launch streams the weights
+// once, so 513 rows run as 257 + 256 rather than 512 + 1)
+static int slab_rows(int T)
 {
-    const int mx = ctx->gemm_impl == 2 ? TC_PAIR_MAX_T : kSlab;
+    const int mx = TC_PAIR_MAX_T;
     const int n = (T + mx - 1) / mx;
     return n > 1 ? (T + n - 1) / n : mx;
 }
 
-// One launch of the selected tensor-core kernel (token groups or CTA pairs).
+// One launch of the tensor-core kernel.
 static cudaError_t launch_tc(const hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *W, const bf16 *X, int T,
                              int N, int K, const EpiParams &ep, TcPartition *part = nullptr)
 {
-    if (ctx->gemm_impl == 2)
-        return launch_gemm_pair(M.m[kind][0], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part, true);
-    return launch_gemm_tc(M.get(kind, T), W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part);
+    return launch_gemm_pair(M.m[kind], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part, true);
 }
 
 // The epilogue parameters of rows [t0, t0 + Tn) of a batch.
@@ -207,8 +187,6 @@ static EpiParams epi_rows(const EpiParams &ep, int t0, int Tn)
     return e;
 }
 
-// W is in the tiled layout; tmW its tensor map (for a slab of kSlab rows
-// when T is larger: the weight slice height depends on the slab's rows).
 // Attention with the tcgen05 chunk kernel, then the decode kernel as its
 // dependent (see attention.h).
 static cudaError_t launch_attention_tc(const AttnParams &ap, const CUtensorMap &tmK, const CUtensorMap &tmV,
@@ -236,20 +214,19 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
 {
     if (ctx->gemm_impl == 0)
         return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
-    const int slab = slab_rows(ctx, T);
-    const bool pair = ctx->gemm_impl == 2;
+    const int slab = slab_rows(T);
     // pair kernel on a product of more tile pairs than CTA pairs: one
     // data-parallel wave with the fused epilogue, the rest stream-K into
     // partials that a reduce pass finishes (gate/up only: its epilogue maps
     // stored rows to features by a plain offset, epi_cols)
-    const int dp_tiles = (pair && ep.mode == EPI_SWIGLU) ? tc_pair_dp_tiles(ctx->fast->rt, N, K) : 0;
+    const int dp_tiles = ep.mode == EPI_SWIGLU ? tc_pair_dp_tiles(ctx->fast->rt, N, K) : 0;
     if (dp_tiles > 0) {
         ctx->n_launches += 2 * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
         for (int t0 = 0; t0 < T; t0 += slab) {
             const int Tn = T - t0 < slab ? T - t0 : slab;
             const EpiParams er = epi_rows(ep, t0, Tn);
             TcPartition part;
-            cudaError_t e = launch_gemm_pair(M.m[kind][0], W, X + (size_t)t0 * K, Tn, N, K, er, ctx->fast->rt,
+            cudaError_t e = launch_gemm_pair(M.m[kind], W, X + (size_t)t0 * K, Tn, N, K, er, ctx->fast->rt,
                                              ctx->stream, &part, true, dp_tiles);
             if (e == cudaSuccess)
                 e = launch_reduce_epi(part, epi_cols(er, dp_tiles * 2 * 128), ctx->stream, true);
@@ -260,12 +237,12 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
     }
     // the pair kernel leaves fp32 partial tiles; a grid-wide pass sums them
     // and applies the fused epilogue
-    const int per_slab = (pair && !tc_pair_data_parallel(ctx->fast->rt, N)) ? 2 : 1;
+    const int per_slab = tc_pair_data_parallel(ctx->fast->rt, N) ? 1 : 2;
     ctx->n_launches += per_slab * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
     for (int t0 = 0; t0 < T; t0 += slab) {
         const int Tn = T - t0 < slab ? T - t0 : slab;
         const EpiParams er = epi_rows(ep, t0, Tn);
-        if (!pair || tc_pair_data_parallel(ctx->fast->rt, N)) {
+        if (tc_pair_data_parallel(ctx->fast->rt, N)) {
             cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, er);
             if (e != cudaSuccess)
                 return e;
@@ -292,7 +269,7 @@ static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const 
                                int K, const bf16 *resid, bf16 *out, const float *gamma, bf16 *norm_out, int *launches)
 {
     const hb_model_config &c = ctx->cfg;
-    const int slab = slab_rows(ctx, T);
+    const int slab = slab_rows(T);
     for (int t0 = 0; t0 < T; t0 += slab) {
         const int Tn = T - t0 < slab ? T - t0 : slab;
         EpiParams pp{};
@@ -304,7 +281,7 @@ static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const 
         if (e != cudaSuccess)
             return e;
         e = launch_reduce_norm(part, Tn, N, resid + (size_t)t0 * N, out + (size_t)t0 * N, gamma,
-                               norm_out + (size_t)t0 * N, c.rms_eps, ctx->stream, ctx->gemm_impl == 2);
+                               norm_out + (size_t)t0 * N, c.rms_eps, ctx->stream, true);
         if (e != cudaSuccess)
             return e;
         *launches += 2;
@@ -328,14 +305,14 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     const LayerMaps &M = ctx->fast->maps[l];
     const int T = b.T, H = c.hidden, d = c.head_dim;
     cudaStream_t s = ctx->stream;
-    const bool tc = ctx->gemm_impl >= 1;
+    const bool tc = ctx->gemm_impl == 2;
 
     // on the tensor-core path norm-1 of every layer but the first was
     // produced by the previous layer's final reduce
     // the step's first kernel also copies the batch plan to the device
     if (!tc || l == l_first) {
         const bool first = l == l_first;
-        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s, ctx->gemm_impl == 2,
+        LK(K_RMSNORM, launch_rmsnorm(x, L.g1, ctx->xn, T, H, c.rms_eps, s, tc,
                                      first ? ctx->meta_src : nullptr, first ? ctx->d_meta : nullptr,
                                      first ? ctx->meta_n16 : 0));
     }
@@ -375,7 +352,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
         ap.part = f->attn_part;
         ap.counters = f->attn_counters;
         ap.err = ctx->err_word;
-        const bool pdl = ctx->gemm_impl == 2;
+        const bool pdl = tc;
         if (ctx->attn_impl == 2)
             LK(K_ATTENTION, launch_attention_tc(ap, f->kv_maps[2 * l], f->kv_maps[2 * l + 1], s, pdl));
         else
@@ -458,16 +435,11 @@ extern "C" int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, 
         f->test_w_elems = need;
     }
     CUtensorMap tm;
-    const bool pair = ctx->gemm_impl == 2;
-    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K, pair ? 128 : tc_weight_box_rows(T)))
+    if (!make_tmap_tiled_weights(&tm, f->test_w, N, K, 128))
         return ctx->set_error(HB_ECUDA, "cuTensorMapEncodeTiled failed");
     ctx->n_launches++;
     if (launch_tile_weights((const bf16 *)W, f->test_w, N, K, 0, 0, ctx->stream) != cudaSuccess)
         return ctx->set_error(HB_ECUDA, "tile launch failed");
-    if (!pair) {
-        LK(K_GEMM_TEST, launch_gemm_tc(tm, f->test_w, (const bf16 *)X, T, N, K, ep, f->rt, ctx->stream));
-        return HB_OK;
-    }
     for (int t0 = 0; t0 < T; t0 += TC_PAIR_MAX_T) {
         const int Tn = T - t0 < TC_PAIR_MAX_T ? T - t0 : TC_PAIR_MAX_T;
         EpiParams pp{};
@@ -486,8 +458,8 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
 {
     if (!ctx)
         return HB_EINVAL;
-    if (gemm_impl < 0 || gemm_impl > 2 || attn_impl < 0 || attn_impl > 2)
-        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl and attn_impl must be 0, 1 or 2");
+    if ((gemm_impl != 0 && gemm_impl != 2) || attn_impl < 0 || attn_impl > 2)
+        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0 or 2, attn_impl 0, 1 or 2");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
     return HB_OK;

@@ -89,18 +89,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
-// Same, delivered to the same shared-memory offset (data and mbarrier) of
-// every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1,
-                                                      uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;
@@ -175,20 +163,6 @@ __device__ __forceinline__ void tma_load_2d_elect(void *dst, const CUtensorMap *
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d_multicast_elect(void *dst, const CUtensorMap *m, uint64_t *bar, int c0,
-                                                            int c1, uint16_t cta_mask)
-{
-    asm volatile(
-        "{\n"
-        ".reg .pred e;\n"
-        "elect.sync _|e, 0xffffffff;\n"
-        "@e cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;\n"
-        "}\n" ::"r"(smem_u32(dst)),
-        "l"((uint64_t)m), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 __device__ __forceinline__ void bulk_prefetch_l2_elect(const void *src, uint32_t bytes)
 {
     asm volatile(
@@ -240,18 +214,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
-// Arrive on the mbarrier at this offset in every CTA of cta_mask once every
-// tcgen05 op issued so far by this thread completes.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Warp-wide forms of mma_bf16 / mma_commit / mma_commit_multicast (see the
+// Warp-wide forms of mma_bf16 / mma_commit (see the
 // issue helpers above).
 __device__ __forceinline__ void mma_bf16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate)
@@ -275,18 +238,6 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t *bar)
         "elect.sync _|e, 0xffffffff;\n"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
         "}\n" ::"r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_multicast_elect(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "{\n"
-        ".reg .pred e;\n"
-        "elect.sync _|e, 0xffffffff;\n"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
-        "}\n" ::"r"(smem_u32(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 

@@ -215,8 +215,8 @@ long long hb_launch_count(hb_ctx *ctx);
 int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int N, int K);
 
 /* Test hook: choose the kernels later calls use.  gemm_impl 0 = reference
- * SIMT GEMM, 1 = tcgen05 GEMM on clusters of token groups, 2 = tcgen05 GEMM
- * on CTA pairs with the 2-SM MMA (default); attn_impl 0 = one CTA per
+ * SIMT GEMM, 2 = tcgen05 GEMM on CTA pairs with the 2-SM MMA (default; any
+ * other value is HB_EINVAL); attn_impl 0 = one CTA per
  * (row, head), 1 = paged attention with mma.sync chunk tiles (default), 2 =
  * paged attention with tcgen05 chunk tiles.  Every setting computes the same
  * function. */
