@@ -291,6 +291,8 @@ typedef struct {
     double *o; /* [T][n_heads d] attention output */
     double *h; /* [T][hidden] after the first residual */
     double *a; /* [T][ffn] silu(g) * u */
+    double *n1; /* [T][hidden] RMSNorm-1 output */
+    double *n2; /* [T][hidden] RMSNorm-2 output */
 } or_aux;
 
 static void row_info(const or_batch *b, int r, int *pos, const int32_t **bt, int *nb)
@@ -392,6 +394,8 @@ int oracle_layer_forward(const or_dims *dm, const or_layer *w, int mirror,
         or_rmsnorm(x_in + (size_t)r * H, w->norm1, H, dm->rms_eps, n1);
         for (int i = 0; i < H; ++i)
             n1[i] = rbf(n1[i], mirror);
+        if (aux && aux->n1)
+            memcpy(aux->n1 + (size_t)r * H, n1, sizeof(double) * (size_t)H);
         or_matvec(w->w_qkv, nqkv, H, n1, qkv);
         for (int hq = 0; hq < nh; ++hq)
             or_rope(qkv + (size_t)hq * d, d, pos, dm->rope_theta);
@@ -436,9 +440,11 @@ int oracle_layer_forward(const or_dims *dm, const or_layer *w, int mirror,
 #pragma omp atomic write
                 err = 1;
             }
+#if OR_MUTATE != 12
             for (int i = 0; i < d; ++i)
                 o[(size_t)r * qd + (size_t)hq * d + i] =
                     rbf(o[(size_t)r * qd + (size_t)hq * d + i], mirror);
+#endif /* planted (12): the mirror keeps o unrounded */
         }
     }
     if (err) {
@@ -477,8 +483,12 @@ int oracle_layer_forward(const or_dims *dm, const or_layer *w, int mirror,
 #endif
         }
         or_rmsnorm(hr, w->norm2, H, dm->rms_eps, n2);
+#if OR_MUTATE != 11
         for (int i = 0; i < H; ++i)
             n2[i] = rbf(n2[i], mirror);
+#endif /* planted (11): the mirror keeps n2 unrounded */
+        if (aux && aux->n2)
+            memcpy(aux->n2 + (size_t)r * H, n2, sizeof(double) * (size_t)H);
         or_matvec(w->w_gate_up, 2 * F, H, n2, gu);
         for (int j = 0; j < F; ++j) {
 #if OR_MUTATE == 9

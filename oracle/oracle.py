@@ -62,7 +62,7 @@ class _Batch(ctypes.Structure):
 
 
 class _Aux(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "h", "a")]
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "h", "a", "n1", "n2")]
 
 
 def load(mutate: int = 0) -> ctypes.CDLL:
@@ -253,8 +253,10 @@ def layer_forward(dims, weights: dict, batch, x_in: np.ndarray, pool: Pool, mirr
                 "v": np.full((T, dims.n_kv_heads * dims.head_dim), np.nan),
                 "o": np.full((T, dims.n_heads * dims.head_dim), np.nan),
                 "h": np.full((T, H), np.nan),
-                "a": np.full((T, dims.ffn), np.nan)}
-        a = _Aux(*[_p(bufs[n]) for n in ("q", "k", "v", "o", "h", "a")])
+                "a": np.full((T, dims.ffn), np.nan),
+                "n1": np.full((T, H), np.nan),
+                "n2": np.full((T, H), np.nan)}
+        a = _Aux(*[_p(bufs[n]) for n in ("q", "k", "v", "o", "h", "a", "n1", "n2")])
     rc = L.oracle_layer_forward(ctypes.byref(dm), ctypes.byref(lw), int(bool(mirror)), _p(pool.k), _p(pool.v),
                                 ctypes.byref(b), _p(xv), _p(y), _p(sel), ctypes.byref(a))
     if rc:

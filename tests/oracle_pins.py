@@ -21,6 +21,9 @@ What pins what:
     (chunked prefill equals full prefill -- SARATHI summary, section 3.4,
     "Chunked-Prefills"), for a prefill, a hybrid batch and a GQA layer.
   * invariants: chunked == monolithic and alone == piggybacked, bit for bit.
+  * mirror mode's rounding points: every stored stage equals the bf16 rounding
+    (frexp-based round-half-even to 8 significant bits) of a textbook fp64
+    recomputation from the previous stored stage.
 """
 from __future__ import annotations
 
@@ -378,6 +381,60 @@ def pin_mirror_close_to_exact(mutate=0):
     ym = orc.layer_forward(dims, w, batch, orc.bf16_round(x), p2, mirror=True, mutate=mutate)
     assert np.array_equal(ym, orc.bf16_round(ym)), "mirror output is not bf16"
     assert np.abs(ym - ye).max() < 0.05 and np.abs(ym - ye).mean() < 0.01
+
+
+def _rb(x):
+    """Round fp64 values to the nearest bf16 value (8 significant bits, ties
+    to even) through frexp and numpy's round-half-even: a formulation that
+    shares nothing with the oracle's bit manipulation."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.round(m * 256.0), e - 8)
+
+
+def _same_after_rounding(stored, exact, what):
+    """stored == _rb(exact), except where exact lies within 1e-12 (relative)
+    of a rounding boundary, where fp64 summation order may decide."""
+    ref = _rb(exact)
+    bad = stored != ref
+    if bad.any():
+        e = exact[bad]
+        edge = _rb(e * (1 + 1e-12)) != _rb(e * (1 - 1e-12))
+        assert edge.all(), f"{what}: {int((~edge).sum())} of {e.size} stored values are not bf16(recomputation)"
+
+
+def pin_mirror_rounding_points(mutate=0):
+    """Mirror mode stores bf16 at n1, q/k after RoPE, v, o, h, n2, a and y:
+    each stored stage is the bf16 rounding of the exact fp64 step applied to
+    the previous stored stage (textbook PyTorch ops), over a 37-token prefill."""
+    dims = PIN_DIMS
+    w = synth.layer_weights(dims, 28, 0, gamma="uniform", std=PIN_STD)
+    n, H, nh, nkv, d, Fd = 37, dims.hidden, dims.n_heads, dims.n_kv_heads, dims.head_dim, dims.ffn
+    x = orc.bf16_round(_seq_rows(28, (1,), n, H))
+    table = synth.allocate_tables(28, (2,), [n], 8)[0]
+    pool = orc.Pool(8, nkv, d)
+    batch = synth.HybridBatch(synth.Seq(0, 0, table), n, [])
+    y, aux = orc.layer_forward(dims, w, batch, x, pool, mirror=True, aux=True, mutate=mutate)
+    T = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    W = {k: textbook._w(w[k]) for k in ("w_qkv", "w_o", "w_gate_up", "w_down", "norm1", "norm2")}
+    n1 = F.rms_norm(T(x), (H,), weight=W["norm1"], eps=dims.rms_eps)
+    _same_after_rounding(aux["n1"], n1.numpy(), "n1")
+    qkv = F.linear(T(aux["n1"]), W["w_qkv"])
+    pos = torch.arange(n)
+    q = textbook.rope_complex(qkv[:, :nh * d].reshape(n, nh, d), pos, dims.rope_theta).reshape(n, -1)
+    k = textbook.rope_complex(qkv[:, nh * d:(nh + nkv) * d].reshape(n, nkv, d), pos, dims.rope_theta).reshape(n, -1)
+    _same_after_rounding(aux["q"], q.numpy(), "q")
+    _same_after_rounding(aux["k"], k.numpy(), "k")
+    _same_after_rounding(aux["v"], qkv[:, (nh + nkv) * d:].numpy(), "v")
+    qh, kh, vh = (T(aux[t]).reshape(n, -1, d).transpose(0, 1)[None] for t in ("q", "k", "v"))
+    o = F.scaled_dot_product_attention(qh, kh, vh, is_causal=True)[0].transpose(0, 1).reshape(n, nh * d)
+    _same_after_rounding(aux["o"], o.numpy(), "o")
+    _same_after_rounding(aux["h"], (T(x) + F.linear(T(aux["o"]), W["w_o"])).numpy(), "h")
+    n2 = F.rms_norm(T(aux["h"]), (H,), weight=W["norm2"], eps=dims.rms_eps)
+    _same_after_rounding(aux["n2"], n2.numpy(), "n2")
+    gu = F.linear(T(aux["n2"]), W["w_gate_up"])
+    _same_after_rounding(aux["a"], (F.silu(gu[:, :Fd]) * gu[:, Fd:]).numpy(), "a")
+    _same_after_rounding(y, (T(aux["h"]) + F.linear(T(aux["a"]), W["w_down"])).numpy(), "y")
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -22,6 +22,8 @@ MUTATIONS = {
     8: "first residual dropped",
     9: "gate and up swapped",
     10: "wrong in-block slot index",
+    11: "mirror mode keeps n2 unrounded",
+    12: "mirror mode keeps o unrounded",
 }
 
 
