@@ -72,7 +72,7 @@ def test_serving_loop_matches_oracle(mode):
         y = f64(x)
         for l in range(2):
             y = orc.layer_forward(dims, weights[l], hb_, y, pools[l], mirror=True)
-        ok, st = compare(gpu, y, layers=2)
+        ok, st = compare(gpu, y)
         assert ok, (steps, st)
         lib.complete()
         ref.complete()

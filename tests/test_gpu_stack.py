@@ -1,92 +1,36 @@
 """Full-size LLaMA-13B stacks (40 layers) on the GPU against the oracle.
 
-Rows of a hybrid batch are independent given the cache (SARATHI summary,
-section 3.4 "Decode-Maximal Batching", how fusion works), and chunk row i at
-offset o reads only the cached prefix and chunk rows 0..i (Figure 6).  So the
-oracle computes, through all forty layers, the first rows of a chunk and any
-decode row on their own, from the same seeded inputs, without the rest of the
-batch; the GPU runs the whole batch in the launch configuration of the
-benchmark.  The rest of the rows are checked for finiteness and, at long
-context, chunked against monolithic prefill ("Chunked-Prefills": chunking
-changes nothing in the result).
-
-Inputs at this size: layer l's matrices are one seeded LLaMA-13B draw with
-their rows rotated by l (forty distinct layers from one draw); gammas 1; a
-sampled sequence's cached K/V at layer l is its seeded draw rotated by l along
-positions; every other sequence's cache holds the constant bf16 1.0 (finite,
-not compared).
+The oracle computes, through all forty layers, the first rows of a chunk and
+any decode row on their own (see stack_helpers); the GPU runs the whole batch
+in the launch configuration of the benchmark.  The rest of the rows are
+checked for finiteness and, at long context, chunked against monolithic
+prefill ("Chunked-Prefills": chunking changes nothing in the result).
 """
 import numpy as np
 import pytest
 
 from chunked_prefill_hybrid_gb300 import native, synth, workloads
 from harness import compare, f64
-from oracle import oracle as orc
+import stack_helpers as sh
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 L = 40
 DIMS = synth.LLAMA_13B.with_layers(L)
-ONE = 0x3F80  # bf16 1.0
-KV_BYTES_PER_TOKEN = L * 2 * DIMS.n_kv_heads * DIMS.head_dim * 2
+KV_BYTES_PER_TOKEN = sh.kv_bytes_per_token(DIMS, L)
 
 
 def _need_gpu_bytes(n_bytes):
-    free, _ = torch.cuda.mem_get_info()
-    if free < n_bytes:
-        pytest.skip(f"needs {n_bytes / 2**30:.0f} GiB of device memory, {free / 2**30:.0f} free")
-
-
-def _layer(base, l):
-    return {k: (np.roll(v, l, axis=0) if v.ndim == 2 else v) for k, v in base.items()}
-
-
-def _prefix(seed, s, l):
-    k, v = synth.prefix_kv(seed, (1000, s.req_id), s.cached, DIMS.n_kv_heads, DIMS.head_dim)
-    return np.roll(k, l, axis=0), np.roll(v, l, axis=0)
+    sh.need_gpu_bytes(torch, pytest, n_bytes)
 
 
 def _upload(ctx, base, seed, sampled):
-    ctx.fill_kv(ONE)
-    dev = {k: workloads.to_device(v) for k, v in base.items()}
-    for l in range(L):
-        ctx.load_layer(l, {k: (torch.roll(v, l, 0) if v.dim() == 2 else v) for k, v in dev.items()})
-        ctx.sync()
-    del dev
-    for s in sampled:
-        if s.cached == 0:
-            continue
-        k0, v0 = synth.prefix_kv(seed, (1000, s.req_id), s.cached, DIMS.n_kv_heads, DIMS.head_dim)
-        kd, vd = workloads.to_device(k0), workloads.to_device(v0)
-        for l in range(L):
-            ctx.append_kv(l, s.block_table, 0, torch.roll(kd, l, 0), torch.roll(vd, l, 0))
-        ctx.sync()
+    sh.upload(torch, ctx, DIMS, L, base, seed, sampled)
 
 
-def _oracle(base, seed, x_rows, chunk, n_chunk_rows, decodes):
-    """The sampled rows through all layers: a chunk of its first n_chunk_rows
-    rows (or none) plus the given decodes, with compact block tables."""
-    seqs = ([chunk] if chunk is not None else []) + list(decodes)
-    lengths = [chunk.cached + n_chunk_rows] if chunk is not None else []
-    lengths += [d.cached + 1 for d in decodes]
-    tables, at = [], 0
-    for n in lengths:
-        nb = synth.blocks_needed(n)
-        tables.append(np.arange(at, at + nb, dtype=np.int32))
-        at += nb
-    small = [synth.Seq(s.req_id, s.cached, t) for s, t in zip(seqs, tables)]
-    sub = synth.HybridBatch(small[0] if chunk is not None else None, n_chunk_rows if chunk is not None else 0,
-                            small[1:] if chunk is not None else small)
-    y = f64(x_rows)
-    for l in range(L):
-        pool = orc.Pool(at, DIMS.n_kv_heads, DIMS.head_dim)
-        for s in small:
-            if s.cached:
-                k, v = _prefix(seed, s, l)
-                pool.write(s.block_table, 0, f64(k), f64(v))
-        y = orc.layer_forward(DIMS, _layer(base, l), sub, y, pool, mirror=True)
-    return y
+def _oracle(base, seed, x_rows, chunk, n_chunk_rows, decodes, mirror=True):
+    return sh.oracle_rows(DIMS, L, base, seed, x_rows, chunk, n_chunk_rows, decodes, mirror=mirror)
 
 
 @pytest.fixture(scope="module")
@@ -120,7 +64,8 @@ def test_llama13b_stack_hybrid_sampled_rows(base_weights, C, D):
     assert np.isfinite(y).all()
     rows = [0, 1] + [C + j for j in picks]
     ref = _oracle(base_weights, seed, x[rows], batch.chunk, 2, [batch.decodes[j] for j in picks])
-    ok, st = compare(y[rows], ref, layers=L)
+    exact = _oracle(base_weights, seed, x[rows], batch.chunk, 2, [batch.decodes[j] for j in picks], mirror=False)
+    ok, st = compare(y[rows], ref, exact)
     assert ok, (C, D, st)
 
 
@@ -165,11 +110,12 @@ def test_llama13b_stack_long_context_chunked_equals_monolithic(base_weights):
     ctx.free()
     assert np.isfinite(chunked).all() and np.isfinite(mono).all() and np.isfinite(dec).all()
     print("prompt", P, "rows bit-identical chunked vs monolithic:", int((chunked == mono[:P]).all(axis=1).sum()))
-    ok, st = compare(chunked, mono[:P], layers=L)
-    assert ok, ("chunked vs monolithic", P, st)
-    ref = _oracle(base_weights, seed, np.concatenate([x[:2], x[P + np.array(picks)]]),
-                  synth.Seq(0, 0, batch.chunk.block_table), 2, [batch.decodes[j] for j in picks])
+    same = (chunked == mono[:P]).all()
+    assert same, ("chunked vs monolithic differ", P, compare(chunked, mono[:P])[1])
+    args = (base_weights, seed, np.concatenate([x[:2], x[P + np.array(picks)]]),
+            synth.Seq(0, 0, batch.chunk.block_table), 2, [batch.decodes[j] for j in picks])
+    ref, exact = _oracle(*args), _oracle(*args, mirror=False)
     for name, got in (("chunked", np.concatenate([chunked[:2], dec[picks]])),
                       ("monolithic", np.concatenate([mono[:2], mono[P + np.array(picks)]]))):
-        ok, st = compare(got, ref, layers=L)
+        ok, st = compare(got, ref, exact, what=name)
         assert ok, (name, P, st)
