@@ -55,6 +55,8 @@ struct TcArgs {
     int qkv_smem;         // pair kernel, whole QKV tiles: stage the RoPE'd tile in shared memory, store coalesced
     int dp_tiles;         // pair kernel: tile pairs 0..dp_tiles-1 go whole to clusters 0..dp_tiles-1 (fused
                           // epilogue); units / grid then cover only the stream-K rest, tile pairs dp_tiles..
+    uint64_t wait_ns;     // wall-clock limit of every mbarrier wait (2 s; shorter only under a test fault)
+    int fault;            // test fault: the odd CTA of pair 0 withholds its first weight-tile copy
 };
 
 // A cluster's unit range [u0, u1) is cut at tile boundaries into segments
@@ -490,7 +492,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (real && u + TC_PREFETCH < sb)
                     bulk_prefetch_l2_hint_elect(wbase + (size_t)(kb + TC_PREFETCH) * TC_BM * TC_BK, TC_W_BYTES, wpol);
                 if (it >= S && (s & rel_mask) == 0 &&
-                    !__all_sync(0xffffffffu, mbar_wait(&empty[s >> rel_shift], ph ^ 1u, abort_flag, TC_WAIT_NS))) {
+                    !__all_sync(0xffffffffu, mbar_wait(&empty[s >> rel_shift], ph ^ 1u, abort_flag, a.wait_ns))) {
                     if (lane == 0) {
                         set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                         *abort_flag = 1;
@@ -502,7 +504,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t fb = full_leader + (uint32_t)(s * 8);
                 if (r == 0)
                     mbar_expect_tx_elect(&full[s], bytes);
-                tma_load_2d_pair_hint_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM, wpol);
+                // test fault: withhold one copy, so the leader's wait for this
+                // stage runs out (nothing else is changed; no copy is left in flight)
+                if (!(a.fault && clu == 0 && r == 1 && it == 0))
+                    tma_load_2d_pair_hint_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM, wpol);
                 if (!waited) {
                     pdl_wait();  // the activations are the previous kernel's output
                     waited = true;
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int k = (it > S ? it - S : 0); k < it; ++k)
             if (k % S % a.rel == 0)
                 mbar_wait(&empty[(k % S) / a.rel], (uint32_t)(k / S) & 1u, ok ? abort_flag : nullptr,
-                          ok ? TC_WAIT_NS : TC_WAIT_NS / 4);
+                          ok ? a.wait_ns : a.wait_ns / 4);
     } else if (warp == 1) {
         if (r == 0) {
             // -------------------------------------------------- MMA issuer
@@ -547,7 +552,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         dcol[sub] = (uint32_t)(j * a.n_sub);
                         if ((seen >> j) & 1u) {
                             if (!__all_sync(0xffffffffu,
-                                            mbar_wait(&sfree[j], (par >> j) & 1u, abort_flag, TC_WAIT_NS))) {
+                                            mbar_wait(&sfree[j], (par >> j) & 1u, abort_flag, a.wait_ns))) {
                                 if (lane == 0) {
                                     set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                                     *abort_flag = 1;
@@ -563,7 +568,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     break;
                 tc_fence_after();
                 for (int u = sa; u < sb; ++u) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, TC_WAIT_NS))) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], ph, abort_flag, a.wait_ns))) {
                         if (lane == 0) {
                             set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                             *abort_flag = 1;
@@ -602,7 +607,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 mma_commit_pair_elect(&empty[(s - 1) >> rel_shift]);
             if (!ok) {
                 mma_commit_pair_elect(drain);
-                mbar_wait(drain, 0, nullptr, TC_WAIT_NS / 4);
+                mbar_wait(drain, 0, nullptr, a.wait_ns / 4);
             }
         }
     } else {
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         prefetch_l2(ep.resid + (size_t)c * a.N + nb);
             }
             if (!__all_sync(0xffffffffu,
-                            mbar_wait(&accf[seg & 3], (uint32_t)(seg >> 2) & 1u, abort_flag, TC_WAIT_NS * 2))) {
+                            mbar_wait(&accf[seg & 3], (uint32_t)(seg >> 2) & 1u, abort_flag, a.wait_ns * 2))) {
                 if (lane == 0 && !*abort_flag) {
                     set_dev_err(ep.err, DERR_MBAR_TIMEOUT);
                     *abort_flag = 1;
@@ -878,7 +883,7 @@ int tc_pair_dp_tiles(const TcRuntime &rt, int N, int K)
 
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
                              const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part, bool pdl,
-                             int dp_tiles)
+                             int dp_tiles, uint64_t fault_wait_ns)
 {
     if (T <= 0)
         return cudaSuccess;
@@ -904,6 +909,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         (dp_tiles > 0 && (long long)(n_mpairs - dp_tiles) * a.nkb < dp_tiles))
         return cudaErrorInvalidValue;
     a.dp_tiles = dp_tiles;
+    a.wait_ns = fault_wait_ns ? fault_wait_ns : TC_WAIT_NS;
+    a.fault = fault_wait_ns ? 1 : 0;
     const long long units = (long long)(n_mpairs - dp_tiles) * a.nkb;  // the stream-K part
     if (units > (1ll << 30) || (long long)n_mpairs * 2 > rt.n_counters)
         return cudaErrorInvalidValue;

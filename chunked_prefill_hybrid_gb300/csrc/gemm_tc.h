@@ -73,9 +73,13 @@ bool tc_pair_data_parallel(const TcRuntime &rt, int N);
 // describes that stream-K part alone (its tile pair 0 is tile pair dp_tiles),
 // for launch_reduce_epi with the epilogue of the features from
 // dp_tiles * 256 on.
+// fault_wait_ns > 0 (test hook only): every wait of this launch gives up
+// after fault_wait_ns, and the odd CTA of CTA pair 0 withholds its first
+// weight-tile copy, so that the even CTA's wait for that stage runs out; the
+// launch then records DERR_MBAR_TIMEOUT, drains, frees TMEM and returns.
 cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
                              const EpiParams &ep, const TcRuntime &rt, cudaStream_t s, TcPartition *part = nullptr,
-                             bool pdl = false, int dp_tiles = 0);
+                             bool pdl = false, int dp_tiles = 0, uint64_t fault_wait_ns = 0);
 // Tile pairs of an N x K product worth running as one data-parallel wave
 // ahead of a stream-K rest: one per CTA pair when the product has more tile
 // pairs than the GPU has CTA pairs and the rest gives every pair at least one

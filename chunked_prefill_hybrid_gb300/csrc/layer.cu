@@ -31,6 +31,7 @@ struct FastPath {
     const int *d_items = nullptr, *d_part_off = nullptr;
     int n_items = 0, n_chunk_items = 0;
     std::vector<CUtensorMap> kv_maps;  // [layer][K, V] pool maps of the tcgen05 chunk attention
+    uint64_t fault_wait_ns = 0;        // armed test fault (hb_test_wait_timeout), 0 = none
 };
 
 static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + HB_MAX_CHUNKS; }
@@ -158,11 +159,14 @@ static int slab_rows(int T)
     return n > 1 ? (T + n - 1) / n : mx;
 }
 
-// One launch of the tensor-core kernel.
-static cudaError_t launch_tc(const hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *W, const bf16 *X, int T,
+// One launch of the tensor-core kernel (a pending test fault goes to the
+// first launch after it was armed).
+static cudaError_t launch_tc(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *W, const bf16 *X, int T,
                              int N, int K, const EpiParams &ep, TcPartition *part = nullptr)
 {
-    return launch_gemm_pair(M.m[kind], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part, true);
+    const uint64_t fault = ctx->fast->fault_wait_ns;
+    ctx->fast->fault_wait_ns = 0;
+    return launch_gemm_pair(M.m[kind], W, X, T, N, K, ep, ctx->fast->rt, ctx->stream, part, true, 0, fault);
 }
 
 // The epilogue parameters of rows [t0, t0 + Tn) of a batch.
@@ -462,5 +466,17 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
         return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0 or 2, attn_impl 0, 1 or 2");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
+    return HB_OK;
+}
+
+extern "C" int hb_test_wait_timeout(hb_ctx *ctx, long long wait_ns)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    if (wait_ns < 100000 || wait_ns > 2000000000ll)
+        return ctx->set_error(HB_EINVAL, "hb_test_wait_timeout: wait_ns must lie in [1e5, 2e9]");
+    if (ctx->gemm_impl != 2)
+        return ctx->set_error(HB_EINVAL, "hb_test_wait_timeout: needs the tensor-core GEMM (gemm_impl 2)");
+    ctx->fast->fault_wait_ns = (uint64_t)wait_ns;
     return HB_OK;
 }

@@ -25,8 +25,8 @@ _NAMES = {0: "HB_OK", -1: "HB_EINVAL", -2: "HB_ERANGE", -3: "HB_ENOMEM", -4: "HB
 # Every symbol include/hb.h declares.
 ABI_SYMBOLS = ["hb_init", "hb_load_layer", "hb_append_kv", "hb_read_kv", "hb_fill_kv", "hb_forward",
                "hb_forward_layers", "hb_forward_host", "hb_sync", "hb_profile", "hb_profile_read",
-               "hb_launch_count", "hb_gemm_test", "hb_debug_read", "hb_set_kernels", "hb_plan", "hb_last_error", "hb_free",
-               "hb_decode_attention_noalloc"]
+               "hb_launch_count", "hb_gemm_test", "hb_debug_read", "hb_set_kernels", "hb_test_wait_timeout", "hb_plan",
+               "hb_last_error", "hb_free", "hb_decode_attention_noalloc"]
 
 
 class HbError(RuntimeError):
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
         "hb_gemm_test": ([vp, vp, vp, vp, ci, ci, ci], ci),
         "hb_debug_read": ([vp, ci, vp, ci], ci),
         "hb_set_kernels": ([vp, ci, ci], ci),
+        "hb_test_wait_timeout": ([vp, ctypes.c_longlong], ci),
         "hb_plan": ([P(ModelConfig), P(BatchSpec), vp, vp, ctypes.c_char_p, ci], ci),
         "hb_last_error": ([vp], ctypes.c_char_p),
         "hb_free": ([vp], None),
@@ -259,6 +260,10 @@ class Context:
 
     def set_kernels(self, gemm_impl: int, attn_impl: int):
         self._check(self.L.hb_set_kernels(self.h, gemm_impl, attn_impl))
+
+    def test_wait_timeout(self, wait_ns: int):
+        """Arm the failure-path test fault in the next tensor-core GEMM launch."""
+        self._check(self.L.hb_test_wait_timeout(self.h, int(wait_ns)))
 
     def debug_read(self, which: int, dst):
         self._check(self.L.hb_debug_read(self.h, which, _ptr(dst), int(dst.shape[0])))

@@ -222,6 +222,20 @@ int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int 
  * function. */
 int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl);
 
+/* Test hook for the failure path: arm a fault in the next tensor-core GEMM
+ * launch of this context (the first layer's QKV projection of the next
+ * forward).  In that launch every mbarrier wait gives up after wait_ns
+ * (in [1e5, 2e9] ns) instead of 2 s, and the second CTA of the first CTA pair
+ * does not issue its first weight-tile copy, so the first CTA's wait for that
+ * pipeline stage runs out.  The kernel then records DERR_MBAR_TIMEOUT in the
+ * device error word, stops issuing, drains its own MMAs, frees its tensor
+ * memory and returns; no copy is left in flight and no memory is touched out
+ * of place.  The forward's output is then undefined and the next hb_sync
+ * returns HB_EDEVICE (and clears the word); the forward after that is
+ * normal.  HB_EINVAL for a wait_ns out of range or without the tensor-core
+ * GEMM.  Nothing on the pages corresponds to this call. */
+int hb_test_wait_timeout(hb_ctx *ctx, long long wait_ns);
+
 /* Test hook: copy an intermediate of the LAST layer run by the latest
  * forward into dst (device memory, bf16 rows of the batch):
  *   which = 0: n1 or n2 (the last RMSNorm output)  [T][hidden]
@@ -258,10 +272,14 @@ int hb_debug_read(hb_ctx *ctx, int which, void *dst, int rows);
  * HB_EINVAL (bad argument), HB_ECUDA (a CUDA call failed).  A row whose
  * ctx_lens entry lies outside [0, max_ctx], or whose table holds a block id
  * outside [0, num_blocks), gets NaN.
- * The first call on each device (with that device current) looks up the
- * array's device address and zeroes its counters on cuda_stream; make that
- * first call before any stream capture.  Every call leaves the counters at
- * zero.  All calls on a device share the array, so calls that can overlap
+ * Every call looks up the array's device address with the device current
+ * (the array's name in host code is not a device address, and a device
+ * reset can move it); the first call on each device, and the first after
+ * such a move, also zeroes the counters on cuda_stream: make the first call
+ * on each device before any stream capture.  Every call leaves the counters
+ * at zero.  Results agree with the decode rows of hb_forward to within one
+ * bf16 step, not bit for bit: this call splits at 256 keys, the forward at
+ * 1024, so their fp32 sums run in different orders.  All calls on a device share the array, so calls that can overlap
  * on the GPU (different streams without ordering) race and give wrong
  * results: order them.  Asynchronous; errors of the kernel itself show as
  * NaN rows, not as a return code. */
