@@ -11,11 +11,14 @@
 // table -- with its scratch (split partials and arrival counters) in a
 // fixed, file-scope device array, so it allocates nothing.
 //
-// The array is resolved with cudaGetSymbolAddress once per device, on the
-// first call made with that device current (which also zeroes the
-// counters); make that first call before any stream capture.  Every call
-// shares the one array: calls that overlap on the GPU race and give wrong
-// results.  Each call leaves the counters at zero again.
+// Every call asks the runtime (cudaGetSymbolAddress, with the device
+// current) where the array lives: the array's name in host code is only a
+// host-side stand-in, and the module -- with the array -- may be loaded at
+// another address after a device reset.  The first call on a device, and the
+// first after the address changed, also zeroes the counters; make the first
+// call on each device before any stream capture.  Every call shares the one
+// array: calls that overlap on the GPU race and give wrong results.  Each
+// call leaves the counters at zero again.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -26,7 +29,9 @@
 namespace hb {
 namespace {
 
-constexpr int NA_SPLIT = 256;         // keys per split at most (the batch path's rule)
+constexpr int NA_SPLIT = 256;         // keys per split at most: small splits keep the fixed partials array
+                                      // small (the batch forward splits at 1024 keys, so its fp32 sums run in
+                                      // another order and the two agree to within one bf16 step)
 constexpr int NA_MAX_PAIRS = 4096;    // decodes x heads
 constexpr int NA_MAX_PARTS = 16384;   // decodes x heads x splits
 constexpr int NA_MAX_D = 128;
@@ -208,22 +213,22 @@ extern "C" int hb_decode_attention_noalloc(const void *q, const void *k_pool, co
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
         return HB_ECUDA;
     cudaStream_t s = (cudaStream_t)cuda_stream;
-    unsigned char *scratch;
+    // the device address of the array, looked up on every call (a host-side
+    // table lookup once the module is loaded); zero the counters whenever it
+    // is new for this device
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_na_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return HB_ECUDA;
+    }
+    unsigned char *scratch = (unsigned char *)p;
     {
         std::lock_guard<std::mutex> lock(g_na_mu);
-        if (!g_na_ptr[dev]) {
-            // once per device: the host-side name of the array is not a
-            // device address; ask the runtime for it, then zero the counters
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_na_scratch) != cudaSuccess || !p) {
-                cudaGetLastError();
+        if (g_na_ptr[dev] != scratch) {
+            if (cudaMemsetAsync(scratch, 0, NA_COUNTER_BYTES, s) != cudaSuccess)
                 return HB_ECUDA;
-            }
-            if (cudaMemsetAsync(p, 0, NA_COUNTER_BYTES, s) != cudaSuccess)
-                return HB_ECUDA;
-            g_na_ptr[dev] = (unsigned char *)p;
+            g_na_ptr[dev] = scratch;
         }
-        scratch = g_na_ptr[dev];
     }
     const dim3 grid((unsigned)(pairs * max_splits));
     if (head_dim == 128)

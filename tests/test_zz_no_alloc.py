@@ -1,6 +1,7 @@
 """hb_decode_attention_noalloc -- decode attention with its scratch in a fixed
-static device array, for callers that cannot allocate -- against the
-attention output of hb_forward's decode rows on the same q and K/V.
+static device array, for callers that cannot allocate -- against the oracle's
+attention on seeded q and K/V, and against the attention output of
+hb_forward's decode rows on the same q and K/V.
 
 The file name sorts last so that a full run calls it after every other GPU
 test in the same process; it also passes alone.
@@ -9,6 +10,7 @@ import numpy as np
 import pytest
 
 from chunked_prefill_hybrid_gb300 import native, synth, workloads
+from oracle import oracle as orc
 
 torch = pytest.importorskip("torch")
 
@@ -112,3 +114,79 @@ def test_noalloc_matches_forward_attention(dims):
     keep = [j for j in range(n) if j != 3]
     assert torch.equal(out[keep], outs[0][keep])
     assert torch.equal(again, outs[0])
+
+
+def _seeded_case(dims, seed, ctxs, num_blocks):
+    """q ~ N(0, 4), a whole pool of K/V ~ N(0, 1) in [num_blocks][n_kv][16][d], shuffled block tables."""
+    n, nh, nkv, hd = len(ctxs), dims.n_heads, dims.n_kv_heads, dims.head_dim
+    q = synth.normal_bf16(seed, (1,), (n, nh, hd), 2.0)
+    kp = synth.normal_bf16(seed, (2,), (num_blocks, nkv, 16, hd))
+    vp = synth.normal_bf16(seed, (3,), (num_blocks, nkv, 16, hd))
+    tables = synth.allocate_tables(seed, (4,), [c + 1 for c in ctxs], num_blocks)
+    stride = max(len(t) for t in tables)
+    bt = np.full((n, stride), -1, np.int32)
+    for j, t in enumerate(tables):
+        bt[j, :len(t)] = t
+    return q, kp, vp, bt
+
+
+def _oracle_rows(dims, q, kp, vp, bt, ctxs):
+    num_blocks, nkv, _, hd = kp.shape
+    pool = orc.Pool(num_blocks, nkv, hd)
+    pool.k[:] = synth.bf16_to_f32(kp).astype(np.float64).transpose(0, 2, 1, 3).reshape(-1, nkv, hd)
+    pool.v[:] = synth.bf16_to_f32(vp).astype(np.float64).transpose(0, 2, 1, 3).reshape(-1, nkv, hd)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    group = dims.n_heads // nkv
+    ref = np.zeros(qf.shape)
+    for j, c in enumerate(ctxs):
+        for h in range(dims.n_heads):
+            ref[j, h] = orc.attention_head(qf[j, h], pool, h // group, bt[j], c)
+    return ref
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dims", [D128, GQA], ids=["d128", "gqa"])
+def test_noalloc_matches_oracle(dims):
+    """Against the oracle's fp64 attention: each output is the bf16 rounding of the fp64 answer, give or
+    take fp32 error, i.e. |got - ref| <= 2^-8 |ref| + 2e-5 (one bf16 step), and the literal 3e-2 / 3e-3
+    bound holds; two calls in a row give the same bytes.  Then one decode's table holds a block id outside
+    the pool (num_blocks, and -1) at a 1100-key, five-split context: that row alone is NaN, and the next
+    good call matches again."""
+    ctxs = CTX
+    num_blocks = sum(synth.blocks_needed(c + 1) for c in ctxs) + 5
+    q, kp, vp, bt = _seeded_case(dims, 41, ctxs, num_blocks)
+    ref = _oracle_rows(dims, q, kp, vp, bt, ctxs)
+    qd, kd, vd, btd = _dev(q), _dev(kp), _dev(vp), torch.from_numpy(bt).cuda()
+    lens = torch.tensor(ctxs, dtype=torch.int32, device="cuda")
+    max_ctx = max(ctxs)
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(qd, NAN16)
+        native.decode_attention_noalloc(qd, kd, vd, btd, lens, max_ctx, out)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    got = _bf(outs[0]).double().cpu().numpy()
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all()
+    assert (err <= 2.0 ** -8 * np.abs(ref) + 2e-5).all(), float((err - 2.0 ** -8 * np.abs(ref)).max())
+    assert err.max() <= 3e-2 and err.mean() <= 3e-3, (err.max(), err.mean())
+
+    j = ctxs.index(1100)
+    for bad_id in (num_blocks, -1):
+        bad = bt.copy()
+        bad[j, 40] = bad_id  # keys 640..655: inside the third 256-key split
+        out = torch.full_like(qd, 0)
+        native.decode_attention_noalloc(qd, kd, vd, torch.from_numpy(bad).cuda(), lens, max_ctx, out)
+        again = torch.full_like(qd, NAN16)
+        native.decode_attention_noalloc(qd, kd, vd, btd, lens, max_ctx, again)
+        torch.cuda.synchronize()
+        g = _bf(out)
+        assert torch.isnan(g[j]).all(), bad_id
+        keep = [i for i in range(len(ctxs)) if i != j]
+        assert torch.equal(out[keep], outs[0][keep]), bad_id
+        assert torch.equal(again, outs[0]), bad_id
