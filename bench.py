@@ -360,6 +360,62 @@ def tile_curve(args, torch, native, workloads, synth, world, rank):
     return 0
 
 
+def prefill_sweep(args, torch, native, workloads, synth, world, rank):
+    """The single-layer comparisons the pages make beside the hybrid batch
+    (LLaMA-13B layer): prefill-only batches of T in {64, ..., 1024} tokens (one
+    request at offset 0; SARATHI summary, section 2, Figure 4a, the prefill
+    plateau at B x L >= 512), decode-only batches of B in {1, 2, 18} at context
+    1024 with their per-token cost against the 1024-token prefill's (Figure 3:
+    200x / 100x / 16.7x on an A6000), and Table 2's three batches of 1024 rows
+    (prefill-only, decode-only of 4, hybrid of 1021 prompt tokens + 3 decodes)
+    with the hybrid's marginal decode cost.  One JSON line."""
+    w = workloads.make("llama13b-prefill-sweep", synth.LLAMA_13B, 2 + rank, 0, 1024, [1024] * 18)
+    ctx = native.Context(workloads.config(w))
+    x = workloads.upload(w, ctx, poison=None)
+    steps = max(10, min(args.steps, 50))
+    chunk, decs = w.batch.chunk, w.batch.decodes
+
+    def timed(b, rows):
+        spec = native.Spec(b)
+        xi = rows.contiguous()
+        yi = torch.empty_like(xi)
+        fn = lambda: ctx.forward(spec, xi, yi)
+        for _ in range(args.warmup):
+            fn()
+        ctx.sync()
+        return max_over_ranks(world, time_steps(torch, ctx, fn, steps, world)) / steps
+
+    prefill = {}
+    for T in (64, 128, 256, 512, 1021, 1024):
+        prefill[T] = timed(synth.HybridBatch(chunk, T, []), x[:T])
+    decode = {}
+    for B in (1, 2, 3, 4, 18):
+        decode[B] = timed(synth.HybridBatch(None, 0, decs[:B]), x[1024:1024 + B])
+    hybrid = timed(synth.HybridBatch(chunk, 1021, decs[:3]), torch.cat([x[:1021], x[1024:1027]]))
+    ctx.free()
+    per_tok_prefill = prefill[1024] / 1024
+    line = {
+        "prefill_sweep": "llama13b-layer", "steps_timed": steps,
+        "prefill_only": [{"T": T, "ms": round(ms, 5), "tok_per_ms": round(T / ms, 1),
+                          "us_per_token": round(ms / T * 1e3, 4)} for T, ms in sorted(prefill.items())],
+        "decode_vs_prefill_per_token": [{"B": B, "ctx": 1024, "ms": round(decode[B], 5),
+                                         "us_per_token": round(decode[B] / B * 1e3, 3),
+                                         "ratio_to_prefill_1024": round(decode[B] / B / per_tok_prefill, 1)}
+                                        for B in (1, 2, 18)],
+        "table2_1024_rows": {"prefill_only_ms": round(prefill[1024], 5), "decode_only_4_ms": round(decode[4], 5),
+                             "hybrid_1021_plus_3_ms": round(hybrid, 5),
+                             "decode_only_us_per_token": round(decode[4] / 4 * 1e3, 3),
+                             "hybrid_marginal_decode_us_per_token": round((hybrid - prefill[1021]) / 3 * 1e3, 3),
+                             "marginal_decode_cost_ratio": round((decode[4] / 4) / ((hybrid - prefill[1021]) / 3), 2)
+                             if hybrid > prefill[1021] else None},
+        "pages_context": {"fig3_ratio_B1_B2_B18": [200, 100, 16.7], "fig4a_plateau_tok_per_ms": 180,
+                          "table2_ms_per_token": {"prefill": 0.229, "decode": 12.49, "hybrid_marginal": 1.2},
+                          "hardware": "A6000, FP16"}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def serve_bench(args, torch, native, workloads, synth, world, rank):
     """LLaMA-33B, 60 layers, serving a closed set of requests present at t = 0:
     prompts uniform in [512, 2048], max_new = max(1, round(P / r)) for each P:D
@@ -551,6 +607,9 @@ def main():
                          "and print one JSON line with throughput, TTFT/ITL/TPOT and iteration uniformity")
     ap.add_argument("--serve-requests", type=int, default=128)
     ap.add_argument("--serve-ratios", default="1,5,10,50", help="P:D ratios r: max_new = max(1, round(P / r))")
+    ap.add_argument("--prefill-sweep", action="store_true",
+                    help="time prefill-only batches (T = 64..1024), decode-only batches (B = 1, 2, 18 at ctx 1024) "
+                         "and the pages' Table 2 batches on one LLaMA-13B layer; one JSON line")
     ap.add_argument("--ncu-case", action="store_true",
                     help="run only the warm-up and --steps hybrid steps, untimed (the case ncu captures)")
     args = ap.parse_args()
@@ -572,6 +631,8 @@ def main():
         return serve_bench(args, torch, native, workloads, synth, world, rank)
     if args.stack:
         return stack_bench(args, torch, native, workloads, synth, world, rank)
+    if args.prefill_sweep:
+        return prefill_sweep(args, torch, native, workloads, synth, world, rank)
 
     w = workloads.llama13b_hybrid(seed=2 + rank)
     dims = w.dims
