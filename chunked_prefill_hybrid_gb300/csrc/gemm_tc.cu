@@ -55,6 +55,8 @@ struct TcArgs {
     int qkv_smem;         // pair kernel, whole QKV tiles: stage the RoPE'd tile in shared memory, store coalesced
     int dp_tiles;         // pair kernel: tile pairs 0..dp_tiles-1 go whole to clusters 0..dp_tiles-1 (fused
                           // epilogue); units / grid then cover only the stream-K rest, tile pairs dp_tiles..
+    int slabs, slab_rows;  // token slabs of the launch (1: all T rows); slab s is rows s*slab_rows..
+    size_t ws_slab;        // workspace floats of one slab group
     uint64_t wait_ns;     // wall-clock limit of every mbarrier wait (2 s; shorter only under a test fault)
     int fault;            // test fault: the odd CTA of pair 0 withholds its first weight-tile copy
 };
@@ -414,9 +416,33 @@ __host__ __device__ inline int pair_smem_bytes(int nsub, int n_sub, int stages)
     return stages * pair_stage_bytes(nsub, n_sub) + TC_PAIR_CTRL + TC_META_BYTES + TC_XP_BYTES + 1024;
 }
 
+// The epilogue parameters of the token rows [t0, t0 + rows) of a launch.
+__device__ __forceinline__ EpiParams epi_slab(const EpiParams &e0, int t0, int rows)
+{
+    EpiParams e = e0;
+    e.T = rows;
+    if (t0) {
+        if (e.pos)
+            e.pos += t0;
+        if (e.slot)
+            e.slot += t0;
+        if (e.q_out)
+            e.q_out += (size_t)t0 * e.n_heads * e.head_dim;
+        if (e.resid)
+            e.resid += (size_t)t0 * e.N;
+        if (e.out)
+            e.out += (size_t)t0 * e.N;
+        if (e.act)
+            e.act += (size_t)t0 * e.ffn;
+        if (e.d32)
+            e.d32 += (size_t)t0 * e.N;
+    }
+    return e;
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a,
-                EpiParams ep)
+                EpiParams ep_all)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -437,8 +463,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = (int)cluster_ctarank();  // 0: the pair's leader
-    const int clu = blockIdx.x >> 1;
+    // CTA pairs of the slab groups are interleaved (pair c of every group
+    // side by side), so they stream the same weight tiles at the same time
+    const int pair_id = blockIdx.x >> 1;
+    const int slab = pair_id % a.slabs;
+    const int clu = pair_id / a.slabs;
     const int cta = clu * 2 + r;
+    const int xrow0 = slab * a.slab_rows;
+    const EpiParams ep = epi_slab(ep_all, xrow0, min(a.slab_rows, a.T - xrow0));
     const int sk_base = a.dp_tiles * a.nkb;
     const int u0 = sk_base + unit_begin(clu, a), u1 = sk_base + unit_begin(clu + 1, a);
     const int rel_mask = a.rel - 1, rel_shift = a.rel == 2 ? 1 : 0;
@@ -506,7 +538,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     mbar_expect_tx_elect(&full[s], bytes);
                 // test fault: withhold one copy, so the leader's wait for this
                 // stage runs out (nothing else is changed; no copy is left in flight)
-                if (!(a.fault && clu == 0 && r == 1 && it == 0))
+                if (!(a.fault && pair_id == 0 && r == 1 && it == 0))
                     tma_load_2d_pair_hint_elect(sw, &tmW, fb, 0, (tile * a.nkb + kb) * TC_BM, wpol);
                 if (!waited) {
                     pdl_wait();  // the activations are the previous kernel's output
@@ -516,7 +548,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int sub = 0; sub < 2; ++sub)
                     if (sub < a.nsub)
                         tma_load_2d_pair_elect(sw + TC_W_BYTES + sub * xhalf * TC_BK * 2, &tmX, fb, kb * TC_BK,
-                                               sub * a.n_sub + r * xhalf);
+                                               xrow0 + sub * a.n_sub + r * xhalf);
                 if (++s == S) {
                     s = 0;
                     ph ^= 1u;
@@ -623,8 +655,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // step's first kernel writes: read them after the wait for it
             pdl_wait();
             for (int c = et; c < a.tg; c += 128) {
-                s_pos[c] = c < a.T ? ep.pos[c] : 0;
-                s_slot[c] = c < a.T ? ep.slot[c] : -1;
+                s_pos[c] = c < ep.T ? ep.pos[c] : 0;
+                s_slot[c] = c < ep.T ? ep.slot[c] : -1;
             }
             epi_bar();
         }
@@ -646,7 +678,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int nb = tile * TC_BM + q * 32;
             if (direct && ep.mode == EPI_RESID) {
                 for (int c = lane; c < a.tg; c += 32)
-                    if (c < a.T && nb < a.N)
+                    if (c < ep.T && nb < a.N)
                         prefetch_l2(ep.resid + (size_t)c * a.N + nb);
             }
             if (!__all_sync(0xffffffffu,
@@ -661,7 +693,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (staged)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the stages' async-proxy use is over
             const int wslot = dp_seg ? 0 : mp - u0 / a.nkb;
-            float *ws_mine = a.ws + ((size_t)cta * a.slots + wslot) * a.tg * TC_BM;
+            float *ws_mine = a.ws + (size_t)slab * a.ws_slab + ((size_t)cta * a.slots + wslot) * a.tg * TC_BM;
             for (int sub = 0; sub < a.nsub; ++sub) {
                 const int j = slot_next;
                 slot_next = slot_next + 1 == a.nslot ? 0 : slot_next + 1;
@@ -851,13 +883,15 @@ size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, cons
 {
     size_t need = 0;
     for (int i = 0; i < n_shapes; ++i)
-        for (int T = 1; T <= max_tokens && T <= TC_PAIR_MAX_T; ++T) {
-            const TcShape sh = tc_pair_shape(T);
+        for (int T = 1; T <= max_tokens && T <= TC_PAIR_MAX_ROWS; ++T) {
+            const int slabs = (T + TC_PAIR_MAX_T - 1) / TC_PAIR_MAX_T;
+            const int rows = slabs > 1 ? ((T + slabs - 1) / slabs + 15) / 16 * 16 : T;
+            const TcShape sh = tc_pair_shape(rows);
             const int n_mpairs = ((Ns[i] + TC_BM - 1) / TC_BM + 1) / 2;
             const int nkb = (Ks[i] + TC_BK - 1) / TC_BK;
             const long long units = (long long)n_mpairs * nkb;
             const int grid = tc_grid(units, num_sms / 2);
-            const size_t n = (size_t)grid * 2 * tc_slots(units, grid, nkb) * sh.tg * TC_BM;
+            const size_t n = (size_t)slabs * grid * 2 * tc_slots(units, grid, nkb) * sh.tg * TC_BM;
             if (n > need)
                 need = n;
         }
@@ -887,11 +921,17 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
 {
     if (T <= 0)
         return cudaSuccess;
-    if (K % 8 != 0 || T > TC_PAIR_MAX_T)
+    if (K % 8 != 0 || T > TC_PAIR_MAX_ROWS)
         return cudaErrorInvalidValue;
-    const TcShape sh = tc_pair_shape(T);
+    // more rows than one CTA pair's TMEM holds: token slabs, each with its
+    // own group of CTA pairs (partials only, no data-parallel tiles)
+    const int slabs = (T + TC_PAIR_MAX_T - 1) / TC_PAIR_MAX_T;
+    const int slab_rows = slabs > 1 ? ((T + slabs - 1) / slabs + 15) / 16 * 16 : T;
+    const TcShape sh = tc_pair_shape(slab_rows);
     TcArgs a = {};
     a.T = T;
+    a.slabs = slabs;
+    a.slab_rows = slab_rows;
     a.N = N;
     a.K = K;
     a.n_mtiles = (N + TC_BM - 1) / TC_BM;
@@ -952,6 +992,9 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         }
         mc = n < rt.num_sms / 2 ? n : rt.num_sms / 2;
     }
+    // every slab runs the launch a single slab would (the same grid, so the
+    // same split of K: a row's result does not depend on the batch); the
+    // slab groups' CTA pairs are interleaved and may take several waves
     a.grid = tc_grid(units, mc);
     if (dp_tiles > 0) {
         // one data-parallel wave (tile pair c whole to cluster c, fused
@@ -971,7 +1014,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
                          : 0;
     }
     a.slots = tc_slots(units, a.grid, a.nkb);
-    if ((size_t)a.grid * 2 * a.slots * a.tg * TC_BM > rt.ws_floats)
+    a.ws_slab = (size_t)a.grid * 2 * a.slots * a.tg * TC_BM;
+    if (a.ws_slab * slabs > rt.ws_floats)
         return cudaErrorInvalidValue;
     if (part) {
         part->ws = rt.ws;
@@ -982,6 +1026,9 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         part->tg = a.tg;
         part->slots = a.slots;
         part->pair = 1;
+        part->slabs = slabs;
+        part->slab_rows = slab_rows;
+        part->ws_slab = a.ws_slab;
     }
     a.ws = rt.ws;
     a.counters = rt.counters;
@@ -989,7 +1036,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
     CUtensorMap tmX;
     if (!encode_2d(&tmX, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)(a.n_sub / 2)))
         return cudaErrorInvalidValue;
-    cfg.gridDim = dim3((unsigned)(a.grid * 2));
+    cfg.gridDim = dim3((unsigned)(a.grid * slabs * 2));
     cudaLaunchAttribute attr2[2] = {attr[0], {}};
     if (pdl) {
         attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

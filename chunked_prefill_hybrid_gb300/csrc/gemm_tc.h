@@ -22,26 +22,33 @@ struct TcRuntime {
     int n_counters = 0;
 };
 
-// Where each CTA of one launch left its fp32 partial tiles.  Units are
-// (weight-tile pair, k-block), split evenly over `grid` CTA pairs; tile pair
-// p covers units [p*nkb, p*nkb+nkb).  CTA r of pair c holds weight tile
-// 2p + r for all T tokens (col = token) at slot (p - first tile pair of c),
-// element [col][feature % 128] of ws + (((c * G + r) * slots + slot) * tg) * 128
-// with G = 2.
+// Where each CTA of one launch left its fp32 partial tiles.  The batch's
+// tokens are cut into `slabs` slabs of slab_rows rows (one slab when T <=
+// TC_PAIR_MAX_T); each slab has its own group of `grid` CTA pairs and its own
+// workspace region of ws_slab floats.  Units are (weight-tile pair, k-block),
+// split evenly over a group's CTA pairs; tile pair p covers units
+// [p*nkb, p*nkb+nkb).  CTA r of pair c of slab s holds weight tile 2p + r for
+// the slab's tokens (col = token - s * slab_rows) at slot (p - first tile pair
+// of c), element [col][feature % 128] of
+// ws + s * ws_slab + (((c * G + r) * slots + slot) * tg) * 128, with G = 2.
 struct TcPartition {
     const float *ws = nullptr;
     int grid = 0, G = 2, units = 0, nkb = 0, tg = 0, slots = 0;
     int pair = 1;
+    int slabs = 1, slab_rows = 1 << 30;
+    size_t ws_slab = 0;
 };
 
 // Unit row (tile pair), CTA rank and token column holding the partials of
-// output (t, feature tile mt) in a partition.
-__host__ __device__ inline void tc_part_loc(const TcPartition &p, int t, int mt, int &urow, int &r, int &col)
+// output (t, feature tile mt) in a partition, and that token's slab region.
+__host__ __device__ inline void tc_part_loc(const TcPartition &p, int t, int mt, int &urow, int &r, int &col,
+                                            const float *&ws)
 {
-    (void)p;
+    const int slab = p.slabs > 1 ? t / p.slab_rows : 0;
     urow = mt >> 1;
     r = mt & 1;
-    col = t;
+    col = t - slab * p.slab_rows;
+    ws = p.ws + (size_t)slab * p.ws_slab;
 }
 
 // Weights in the tiled layout [n_tile][k_block][128][64] (zero padded).
@@ -54,13 +61,19 @@ bool make_tmap_kv_pool(CUtensorMap *m, const void *pool, int num_blocks, int n_k
 // The tiled weights as a TMA map of boxes of box_rows (128) x 64 elements.
 bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, int box_rows);
 
-// Largest batch one pair-kernel launch takes (callers cut larger ones).
+// Largest token slab of one CTA pair (its TMEM holds 512 fp32 columns).  A
+// launch of more rows, up to TC_PAIR_MAX_SLABS slabs, runs every slab in one
+// grid, slab groups interleaved so that the pairs reading the same weight
+// tile for different slabs run side by side and the weights leave HBM once.
 constexpr int TC_PAIR_MAX_T = 512;
+constexpr int TC_PAIR_MAX_SLABS = 4;
+constexpr int TC_PAIR_MAX_ROWS = TC_PAIR_MAX_T * TC_PAIR_MAX_SLABS;
 TcShape tc_pair_shape(int T);
 size_t tc_pair_workspace_floats(int num_sms, int max_tokens, const int *Ns, const int *Ks, int n_shapes);
 
-// The same product on CTA pairs with the 2-SM MMA (T <= TC_PAIR_MAX_T);
-// tmW must use 128-row boxes.  With ep.mode EPI_PARTIAL the work is split
+// The same product on CTA pairs with the 2-SM MMA (T <= TC_PAIR_MAX_ROWS;
+// more than TC_PAIR_MAX_T rows only with ep.mode EPI_PARTIAL and no
+// data-parallel tiles); tmW must use 128-row boxes.  With ep.mode EPI_PARTIAL the work is split
 // stream-K and every CTA leaves fp32 partials (part says where); with a
 // fused epilogue the launch is data-parallel (one whole tile pair per CTA
 // pair, which tc_pair_data_parallel says is worthwhile and possible).

@@ -149,12 +149,13 @@ int hb_plan_fast_path(hb_ctx *ctx, const Plan &p, int *hm, size_t &at, BatchDev 
             return ctx->set_error(HB_ECUDA, "launch %s failed: %s", kKindNames[kind], cudaGetErrorString(e_)); \
     } while (0)
 
-// rows per launch of the tensor-core kernel for a batch of T rows: the
-// fewest launches, with their rows balanced (each launch streams the weights
-// once, so 513 rows run as 257 + 256 rather than 512 + 1)
-static int slab_rows(int T)
+// rows per launch of the tensor-core kernel for a batch of T rows: one
+// launch takes up to TC_PAIR_MAX_ROWS rows (slabs of up to TC_PAIR_MAX_T
+// rows, each with the weights read once from HBM); larger batches run as the
+// fewest launches, with their rows balanced
+static int launch_rows(int T)
 {
-    const int mx = TC_PAIR_MAX_T;
+    const int mx = TC_PAIR_MAX_ROWS;
     const int n = (T + mx - 1) / mx;
     return n > 1 ? (T + n - 1) / n : mx;
 }
@@ -218,64 +219,59 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
 {
     if (ctx->gemm_impl == 0)
         return launch_gemm_simt(X, W, T, N, K, true, ep, ctx->stream);
-    const int slab = slab_rows(T);
+    const int rows = launch_rows(T);
     // pair kernel on a product of more tile pairs than CTA pairs: one
     // data-parallel wave with the fused epilogue, the rest stream-K into
     // partials that a reduce pass finishes (gate/up only: its epilogue maps
-    // stored rows to features by a plain offset, epi_cols)
+    // stored rows to features by a plain offset, epi_cols); a product that
+    // fits the CTA pairs runs data-parallel with the fused epilogue; else
+    // every tile stream-K into partials and a reduce pass with the epilogue
     const int dp_tiles = ep.mode == EPI_SWIGLU ? tc_pair_dp_tiles(ctx->fast->rt, N, K) : 0;
-    if (dp_tiles > 0) {
-        ctx->n_launches += 2 * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
-        for (int t0 = 0; t0 < T; t0 += slab) {
-            const int Tn = T - t0 < slab ? T - t0 : slab;
-            const EpiParams er = epi_rows(ep, t0, Tn);
+    const bool dp = dp_tiles == 0 && tc_pair_data_parallel(ctx->fast->rt, N);
+    int launches = 0;
+    for (int t0 = 0; t0 < T; t0 += rows) {
+        const int Tn = T - t0 < rows ? T - t0 : rows;
+        const EpiParams er = epi_rows(ep, t0, Tn);
+        cudaError_t e;
+        if (dp_tiles > 0) {
             TcPartition part;
-            cudaError_t e = launch_gemm_pair(M.m[kind], W, X + (size_t)t0 * K, Tn, N, K, er, ctx->fast->rt,
-                                             ctx->stream, &part, true, dp_tiles);
+            const uint64_t fault = ctx->fast->fault_wait_ns;
+            ctx->fast->fault_wait_ns = 0;
+            e = launch_gemm_pair(M.m[kind], W, X + (size_t)t0 * K, Tn, N, K, er, ctx->fast->rt, ctx->stream, &part,
+                                 true, dp_tiles, fault);
             if (e == cudaSuccess)
                 e = launch_reduce_epi(part, epi_cols(er, dp_tiles * 2 * 128), ctx->stream, true);
-            if (e != cudaSuccess)
-                return e;
+            launches += 2;
+        } else if (dp) {
+            e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, er);
+            launches += 1;
+        } else {
+            EpiParams pp{};
+            pp.mode = EPI_PARTIAL;
+            pp.T = Tn;
+            pp.N = N;
+            pp.err = ep.err;
+            TcPartition part;
+            e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, pp, &part);
+            if (e == cudaSuccess)
+                e = launch_reduce_epi(part, er, ctx->stream, true);
+            launches += 2;
         }
-        return cudaSuccess;
-    }
-    // the pair kernel leaves fp32 partial tiles; a grid-wide pass sums them
-    // and applies the fused epilogue
-    const int per_slab = tc_pair_data_parallel(ctx->fast->rt, N) ? 1 : 2;
-    ctx->n_launches += per_slab * ((T + slab - 1) / slab) - 1;  // one is counted by the caller
-    for (int t0 = 0; t0 < T; t0 += slab) {
-        const int Tn = T - t0 < slab ? T - t0 : slab;
-        const EpiParams er = epi_rows(ep, t0, Tn);
-        if (tc_pair_data_parallel(ctx->fast->rt, N)) {
-            cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, er);
-            if (e != cudaSuccess)
-                return e;
-            continue;
-        }
-        EpiParams pp{};
-        pp.mode = EPI_PARTIAL;
-        pp.T = Tn;
-        pp.N = N;
-        pp.err = ep.err;
-        TcPartition part;
-        cudaError_t e = launch_tc(ctx, M, kind, W, X + (size_t)t0 * K, Tn, N, K, pp, &part);
-        if (e == cudaSuccess)
-            e = launch_reduce_epi(part, er, ctx->stream, true);
         if (e != cudaSuccess)
             return e;
     }
+    ctx->n_launches += launches - 1;  // one is counted by the caller
     return cudaSuccess;
 }
 
-// Tensor-core GEMM leaving partials, then the fused reduce + residual (+ norm),
-// slab by slab.
+// Tensor-core GEMM leaving partials, then the fused reduce + residual (+ norm).
 static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X, const bf16 *W, int T, int N,
                                int K, const bf16 *resid, bf16 *out, const float *gamma, bf16 *norm_out, int *launches)
 {
     const hb_model_config &c = ctx->cfg;
-    const int slab = slab_rows(T);
-    for (int t0 = 0; t0 < T; t0 += slab) {
-        const int Tn = T - t0 < slab ? T - t0 : slab;
+    const int rows = launch_rows(T);
+    for (int t0 = 0; t0 < T; t0 += rows) {
+        const int Tn = T - t0 < rows ? T - t0 : rows;
         EpiParams pp{};
         pp.mode = EPI_PARTIAL;
         pp.T = Tn;
@@ -444,8 +440,8 @@ extern "C" int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, 
     ctx->n_launches++;
     if (launch_tile_weights((const bf16 *)W, f->test_w, N, K, 0, 0, ctx->stream) != cudaSuccess)
         return ctx->set_error(HB_ECUDA, "tile launch failed");
-    for (int t0 = 0; t0 < T; t0 += TC_PAIR_MAX_T) {
-        const int Tn = T - t0 < TC_PAIR_MAX_T ? T - t0 : TC_PAIR_MAX_T;
+    for (int t0 = 0; t0 < T; t0 += TC_PAIR_MAX_ROWS) {
+        const int Tn = T - t0 < TC_PAIR_MAX_ROWS ? T - t0 : TC_PAIR_MAX_ROWS;
         EpiParams pp{};
         pp.mode = EPI_PARTIAL;
         pp.T = Tn;

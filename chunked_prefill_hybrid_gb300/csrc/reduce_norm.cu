@@ -55,7 +55,8 @@ template <int NF, int MAXC>
 __device__ __forceinline__ void rd_sum(const TcPartition &p, const RdTab &tab, int t, int n0, float (&acc)[NF])
 {
     int ur, r, col;
-    tc_part_loc(p, t, n0 >> 7, ur, r, col);
+    const float *ws;
+    tc_part_loc(p, t, n0 >> 7, ur, r, col, ws);
     const int c_lo = tab.clo[ur], c_hi = tab.chi[ur];
 #pragma unroll
     for (int k = 0; k < NF; ++k)
@@ -68,7 +69,7 @@ __device__ __forceinline__ void rd_sum(const TcPartition &p, const RdTab &tab, i
             if (c <= c_hi) {
                 const int slot = ur - tab.first[c];
                 const float4 *src = reinterpret_cast<const float4 *>(
-                    p.ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
+                    ws + ((((size_t)c * p.G + r) * p.slots + slot) * p.tg + col) * 128 + (n0 & 127));
 #pragma unroll
                 for (int e = 0; e < NF / 4; ++e)
                     v[i][e] = __ldcg(src + e);
