@@ -1,6 +1,8 @@
 // common.cuh -- shared device-side definitions of the hybrid-batch library.
 #pragma once
 
+#include <mutex>
+#include <unordered_set>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -52,6 +54,26 @@ struct BatchDev {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Every kernel of the library asks for the largest shared-memory carveout.
+// An SM's split between L1 and shared memory is chosen when a CTA lands on
+// it while it is idle, from that kernel's preference, and a CTA of another
+// kernel can join only within that split: with one preference for all, the
+// CTAs of consecutive kernels (the chunk tiles and the decode splits, a
+// GEMM and its reduce pass) share SMs whichever kernel arrived first.
+inline cudaError_t max_carveout(const void *kernel)
+{
+    static std::mutex mu;
+    static std::unordered_set<const void *> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(kernel))
+        return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        done.insert(kernel);
+    return e;
+}
+
 // Launch a kernel, with the programmatic stream-serialization attribute
 // when pdl is set (the kernel must then call pdl_wait before it reads what
 // the previous kernel on the stream writes).
@@ -59,6 +81,9 @@ template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                                  cudaStream_t s, Args... args)
 {
+    const cudaError_t ce = max_carveout((const void *)kernel);
+    if (ce != cudaSuccess)
+        return ce;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

@@ -966,6 +966,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
     static int configured = 0;
     if (configured < rt.max_smem) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, rt.max_smem);
+        if (e == cudaSuccess)
+            e = max_carveout((const void *)k_gemm_pair);
         if (e != cudaSuccess)
             return e;
         configured = rt.max_smem;
