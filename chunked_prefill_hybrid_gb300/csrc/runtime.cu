@@ -693,6 +693,72 @@ extern "C" int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const voi
     return hb_sync(ctx);
 }
 
+// The first asynchronous call of a context makes its input ring.
+static int async_setup(hb_ctx *ctx)
+{
+    if (ctx->copy_stream)
+        return HB_OK;
+    const size_t bytes = (size_t)ctx->cfg.max_tokens * ctx->cfg.hidden * sizeof(bf16);
+    int rc;
+    if ((rc = ctx_alloc(ctx, (void **)&ctx->async_in[0], bytes)) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->async_in[1], bytes)))
+        return rc;
+    for (int k = 0; k < 2; ++k)
+        if (cudaEventCreateWithFlags(&ctx->in_ready[k], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ctx->in_free[k], cudaEventDisableTiming) != cudaSuccess)
+            return ctx->set_error(HB_ECUDA, "cudaEventCreate failed");
+    if (cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        ctx->copy_stream = nullptr;
+        return ctx->set_error(HB_ECUDA, "cudaStreamCreate failed");
+    }
+    return HB_OK;
+}
+
+extern "C" int hb_forward_host_async(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in_host,
+                                     void *x_out_host)
+{
+    if (!ctx)
+        return HB_EINVAL;
+    if (!x_in_host || !x_out_host)
+        return ctx->set_error(HB_EINVAL, "NULL host buffer");
+    std::string e;
+    int T = 0;
+    int rc = spec_rows(ctx->cfg, spec, &T, &e);
+    if (rc)
+        return ctx->set_error(rc, "%s", e.c_str());
+    if ((rc = async_setup(ctx)))
+        return rc;
+    // the output must be page-locked memory the GPU can address (the last
+    // kernel writes it in place)
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, x_out_host) != cudaSuccess) {
+        cudaGetLastError();
+        return ctx->set_error(HB_EINVAL, "x_out_host is not page-locked memory the GPU can address");
+    }
+    if (pa.type != cudaMemoryTypeHost || !pa.devicePointer || (uintptr_t)pa.devicePointer % 16 != 0)
+        return ctx->set_error(HB_EINVAL, "x_out_host must be 16-byte aligned page-locked memory the GPU can address");
+    void *y = pa.devicePointer;
+    // input slot k: its copy waits for the step that last read it, runs on
+    // the copy stream while the previous step computes, and the step waits
+    // for the copy
+    const int k = ctx->in_i ^= 1;
+    const size_t bytes = (size_t)T * ctx->cfg.hidden * sizeof(bf16);
+    if (ctx->in_used[k])
+        CK(cudaStreamWaitEvent(ctx->copy_stream, ctx->in_free[k], 0));
+    CK(cudaMemcpyAsync(ctx->async_in[k], x_in_host, bytes, cudaMemcpyHostToDevice, ctx->copy_stream));
+    CK(cudaEventRecord(ctx->in_ready[k], ctx->copy_stream));
+    CK(cudaStreamWaitEvent(ctx->stream, ctx->in_ready[k], 0));
+    BatchDev b;
+    if ((rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->async_in[k], y, b)) ||
+        (rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->async_in[k], y))) {
+        cudaStreamSynchronize(ctx->stream);  // nothing of this call is left in flight
+        return rc;
+    }
+    CK(cudaEventRecord(ctx->in_free[k], ctx->stream));
+    ctx->in_used[k] = true;
+    return HB_OK;
+}
+
 extern "C" int hb_sync(hb_ctx *ctx)
 {
     if (!ctx)
@@ -783,6 +849,16 @@ extern "C" void hb_free(hb_ctx *ctx)
     if (!ctx)
         return;
     cudaStreamSynchronize(ctx->stream);
+    if (ctx->copy_stream) {
+        cudaStreamSynchronize(ctx->copy_stream);
+        cudaStreamDestroy(ctx->copy_stream);
+    }
+    for (int k = 0; k < 2; ++k) {
+        if (ctx->in_ready[k])
+            cudaEventDestroy(ctx->in_ready[k]);
+        if (ctx->in_free[k])
+            cudaEventDestroy(ctx->in_free[k]);
+    }
     hb_free_fast_path(ctx);
     for (void *p : ctx->allocations)
         cudaFree(p);

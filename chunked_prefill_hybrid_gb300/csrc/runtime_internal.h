@@ -75,6 +75,14 @@ struct hb_ctx {
     float2 *rope = nullptr;
     hb::bf16 *xn = nullptr, *q = nullptr, *attn_o = nullptr, *h = nullptr, *act = nullptr;
     hb::bf16 *xa = nullptr, *xb = nullptr, *host_in = nullptr, *host_out = nullptr;
+    // hb_forward_host_async: a ring of two device input buffers filled on
+    // copy_stream (in_ready[k] behind the copy, in_free[k] behind the step
+    // that read slot k), made on the first asynchronous call
+    hb::bf16 *async_in[2] = {nullptr, nullptr};
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t in_ready[2] = {nullptr, nullptr}, in_free[2] = {nullptr, nullptr};
+    bool in_used[2] = {false, false};
+    int in_i = 1;
     int *err_word = nullptr;
     int *h_err = nullptr;  // pinned: the error word read back with the stream's work
 

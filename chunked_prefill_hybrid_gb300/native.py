@@ -24,7 +24,7 @@ _NAMES = {0: "HB_OK", -1: "HB_EINVAL", -2: "HB_ERANGE", -3: "HB_ENOMEM", -4: "HB
 
 # Every symbol include/hb.h declares.
 ABI_SYMBOLS = ["hb_init", "hb_load_layer", "hb_append_kv", "hb_read_kv", "hb_fill_kv", "hb_forward",
-               "hb_forward_layers", "hb_forward_host", "hb_sync", "hb_profile", "hb_profile_read",
+               "hb_forward_layers", "hb_forward_host", "hb_forward_host_async", "hb_sync", "hb_profile", "hb_profile_read",
                "hb_launch_count", "hb_gemm_test", "hb_debug_read", "hb_set_kernels", "hb_test_wait_timeout", "hb_plan",
                "hb_last_error", "hb_free", "hb_decode_attention_noalloc"]
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "hb_forward": ([vp, P(BatchSpec), vp, vp], ci),
         "hb_forward_layers": ([vp, P(BatchSpec), ci, ci, vp, vp], ci),
         "hb_forward_host": ([vp, P(BatchSpec), vp, vp], ci),
+        "hb_forward_host_async": ([vp, P(BatchSpec), vp, vp], ci),
         "hb_sync": ([vp], ci),
         "hb_profile": ([vp, ci], ci),
         "hb_profile_read": ([vp, vp, vp, vp, ci], ci),
@@ -231,6 +232,10 @@ class Context:
 
     def forward_host_ptr(self, spec: Spec, x_in_ptr: int, x_out_ptr: int):
         self._check(self.L.hb_forward_host(self.h, ctypes.byref(spec.c), x_in_ptr, x_out_ptr))
+
+    def forward_host_async_ptr(self, spec: Spec, x_in_ptr: int, x_out_ptr: int):
+        """hb_forward_host_async: returns once enqueued; read x_out after sync()."""
+        self._check(self.L.hb_forward_host_async(self.h, ctypes.byref(spec.c), x_in_ptr, x_out_ptr))
 
     def sync(self):
         self._check(self.L.hb_sync(self.h))

@@ -4,6 +4,9 @@ stream.  The same kernels run on the same rows as hb_forward, so the two
 outputs are bit-identical; hb_forward itself is checked against the oracle
 in the parity tests.  A batch that the host plan rejects after the input
 copy has started comes back as an error with the output buffer untouched.
+hb_forward_host_async does the same without waiting: a sequence of calls on
+different batches, with one hb_sync at the end, gives every batch's
+hb_forward result.
 """
 import numpy as np
 import pytest
@@ -63,4 +66,37 @@ def test_rejected_batch_leaves_output_untouched():
     spec.dbt[0, 0] = good
     ctx.forward_host(spec, xin, yout)  # the context is still usable
     assert np.array_equal(yout, want)
+    ctx.free()
+
+
+def test_async_host_calls_equal_device_path():
+    """Five batches of different shapes (chunks, decodes, both), each from its own pinned input into its own
+    pinned output, submitted back to back with one sync at the end; the input ring of two device buffers is
+    reused three times over."""
+    w = workloads.make("host-async", synth.TINY, 31, 40, 48, [20, 90, 300], n_layers=2)
+    ctx = native.Context(workloads.config(w))
+    workloads.upload(w, ctx, poison=None)
+    C, decs, chunk = w.batch.chunk_len, list(w.batch.decodes), w.batch.chunk
+    batches = [synth.HybridBatch(chunk, C, decs), synth.HybridBatch(None, 0, decs[:2]),
+               synth.HybridBatch(chunk, 16, []), synth.HybridBatch(chunk, 7, decs[1:]),
+               synth.HybridBatch(None, 0, decs)]
+    rows = []
+    xs = np.ascontiguousarray(w.x).view(np.uint16)
+    for b in batches:
+        idx = list(range(b.chunk_len)) + [C + decs.index(d) for d in b.decodes]
+        rows.append(np.ascontiguousarray(xs[idx]))
+    want = [_device_out(ctx, native.Spec(b), workloads.to_device(r)) for b, r in zip(batches, rows)]
+    specs = [native.Spec(b) for b in batches]
+    xh = [torch.from_numpy(r.view(np.int16).copy()).pin_memory() for r in rows]
+    yh = [torch.full_like(t, 0x7FC0).pin_memory() for t in xh]
+    for sp, a, b in zip(specs, xh, yh):
+        ctx.forward_host_async_ptr(sp, a.data_ptr(), b.data_ptr())
+    ctx.sync()
+    for i, (b, got) in enumerate(zip(want, yh)):
+        assert np.array_equal(got.numpy().view(np.uint16), b), i
+    # an output buffer the GPU cannot address is refused before anything is enqueued
+    with pytest.raises(native.HbError) as e:
+        ctx.forward_host_async_ptr(specs[0], xh[0].data_ptr(), np.zeros_like(rows[0]).ctypes.data)
+    assert e.value.code == native.HB_EINVAL
+    ctx.sync()
     ctx.free()
