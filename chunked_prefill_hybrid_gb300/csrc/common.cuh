@@ -126,7 +126,7 @@ struct EpiParams {
     float *d32;
 };
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // One output pair (t, n..n+1), n even.
 __device__ __forceinline__ void epi_pair(const EpiParams &p, int t, int n, float a0, float a1)
