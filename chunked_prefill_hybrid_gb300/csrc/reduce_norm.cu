@@ -97,8 +97,11 @@ __host__ __device__ inline int rd_urows(const TcPartition &p, int N)
 }
 
 // One thread per 8-feature group of the row (blockDim = groups rounded up
-// to whole warps, at most 1024 = hidden 8192).
-__global__ void __launch_bounds__(1024) k_reduce_norm(RnArgs a)
+// to whole warps, at most 1024 = hidden 8192).  TWO: rows of at most 5120
+// features (640 threads) with registers bounded so that two CTAs share an
+// SM, and a pass over T <= 2 x (SM count) rows runs in one wave.
+template <bool TWO>
+__global__ void __launch_bounds__(TWO ? 640 : 1024, TWO ? 2 : 1) k_reduce_norm(RnArgs a)
 {
     __shared__ RdTab tab;
     __shared__ float red[32];
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(1024) k_reduce_norm(RnArgs a)
     float ss = 0.f;
     if (n0 < a.N) {
         float acc[8];
-        rd_sum<8, 4>(p, tab, t, n0, acc);
+        rd_sum<8, TWO ? 2 : 4>(p, tab, t, n0, acc);
         const uint4 rv = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
         const bf16 *re = reinterpret_cast<const bf16 *>(&rv);
 #pragma unroll
@@ -192,7 +195,8 @@ cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16
         return cudaErrorInvalidValue;
     RnArgs a{part, T, N, resid, out, gamma, norm_out, eps};
     const int threads = ((N / 8) + 31) / 32 * 32;
-    cudaError_t e = launch_kernel(pdl, k_reduce_norm, dim3(T), dim3(threads), 0, s, a);
+    cudaError_t e = threads <= 640 ? launch_kernel(pdl, k_reduce_norm<true>, dim3(T), dim3(threads), 0, s, a)
+                                   : launch_kernel(pdl, k_reduce_norm<false>, dim3(T), dim3(threads), 0, s, a);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
