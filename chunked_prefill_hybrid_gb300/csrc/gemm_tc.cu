@@ -835,6 +835,11 @@ bool make_tmap_tiled_weights(CUtensorMap *m, const void *tiled, int N, int K, in
     return encode_2d(m, tiled, TC_BK, npad * nkb, TC_BK * 2, TC_BK, (uint32_t)box_rows);
 }
 
+bool make_tmap_rows(CUtensorMap *m, const void *X, int K, int T, int box_rows)
+{
+    return encode_2d(m, X, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, TC_BK, (uint32_t)box_rows);
+}
+
 // The paged K or V pool [num_blocks][n_kv][16][d] as a 2D tensor of
 // num_blocks * n_kv * 16 rows of d elements, in boxes of 16 rows x 64
 // elements (128-byte swizzle): one box is half (d = 128) or all (d = 64) of

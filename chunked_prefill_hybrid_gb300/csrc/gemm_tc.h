@@ -99,6 +99,28 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
 // k-block; else 0.
 int tc_pair_dp_tiles(const TcRuntime &rt, int N, int K);
 
+// The activations X [T][K] bf16 as a TMA map of boxes of box_rows x 64 elements.
+bool make_tmap_rows(CUtensorMap *m, const void *X, int K, int T, int box_rows);
+
+// Split-K linear op with the residual add fused (gemm_ksplit.cu), for
+// products whose K is long against the GPU's CTA pairs (the O and down
+// projections): a cluster of three CTA pairs owns one 256-row weight-tile
+// pair, each pair a third of K; the three fp32 accumulators are summed in
+// pair order through distributed shared memory and
+//   out[t][n] = bf16(resid[t][n] + acc[t][n]),
+//   ss[n / 128][t] = sum over the tile's 128 features of out[t][n]^2 (fp32),
+// (ss: [N / 128][ss_ld], may be null).  T <= TC_PAIR_MAX_T, N % 256 == 0,
+// K % 64 == 0.  Returns cudaErrorNotSupported, launching nothing, when the
+// shape or the GPU's cluster occupancy does not fit; the caller then uses
+// the stream-K path.
+cudaError_t launch_gemm_ksplit(const CUtensorMap &tmW, const bf16 *W_tiled, const bf16 *X, int T, int N, int K,
+                               const bf16 *resid, bf16 *out, float *ss, int ss_ld, int *err, const TcRuntime &rt,
+                               cudaStream_t s, bool pdl);
+// norm_out[t] = bf16(h[t] * rsqrt(sum_i ss[i][t] / N + eps) * gamma), the
+// tiles' partial sums of squares added in tile order.
+cudaError_t launch_norm_apply(const bf16 *h, const float *ss, int n_tiles, int ss_ld, const float *gamma, float eps,
+                              bf16 *norm_out, int T, int N, cudaStream_t s, bool pdl);
+
 // out = bf16(resid + sum of the partial tiles of `part`) for T x N outputs;
 // if gamma: norm_out = bf16(out * rsqrt(mean(out^2) + eps) * gamma) per row.
 cudaError_t launch_reduce_norm(const TcPartition &part, int T, int N, const bf16 *resid, bf16 *out,

@@ -32,6 +32,7 @@ struct FastPath {
     int n_items = 0, n_chunk_items = 0;
     std::vector<CUtensorMap> kv_maps;  // [layer][K, V] pool maps of the tcgen05 chunk attention
     uint64_t fault_wait_ns = 0;        // armed test fault (hb_test_wait_timeout), 0 = none
+    float *ss = nullptr;               // [hidden / 128][max_tokens] partial sums of squares (split-K path)
 };
 
 static size_t max_seqs(const hb_model_config &c) { return (size_t)c.max_decodes + HB_MAX_CHUNKS; }
@@ -81,6 +82,11 @@ int hb_init_fast_path(hb_ctx *ctx)
         }
         if (cudaMemset(f->attn_counters, 0, cnts * sizeof(int)) != cudaSuccess)
             return ctx->set_error(HB_ECUDA, "cudaMemset failed");
+        const size_t ssn = ((size_t)c.hidden / 128 + 1) * c.max_tokens;
+        if (cudaMalloc((void **)&f->ss, ssn * sizeof(float)) != cudaSuccess) {
+            cudaGetLastError();
+            return ctx->set_error(HB_ENOMEM, "split-K workspace allocation failed");
+        }
         f->items.resize(2 * max_items(c));
         f->part_off.resize(max_seqs(c));
     }
@@ -114,6 +120,7 @@ void hb_free_fast_path(hb_ctx *ctx)
         cudaFree(ctx->fast->test_w);
         cudaFree(ctx->fast->attn_part);
         cudaFree(ctx->fast->attn_counters);
+        cudaFree(ctx->fast->ss);
     }
     delete ctx->fast;
     ctx->fast = nullptr;
@@ -264,12 +271,39 @@ static cudaError_t gemm(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X
     return cudaSuccess;
 }
 
-// Tensor-core GEMM leaving partials, then the fused reduce + residual (+ norm).
+// out = resid + X W^T (+ norm_out = RMSNorm(out) * gamma).  gemm_impl 3:
+// the split-K cluster kernel with the residual fused, then the norm pass;
+// else (and where the split-K kernel does not fit) the tensor-core GEMM
+// leaving stream-K partials, then the fused reduce + residual (+ norm).
 static cudaError_t gemm_reduce(hb_ctx *ctx, const LayerMaps &M, int kind, const bf16 *X, const bf16 *W, int T, int N,
                                int K, const bf16 *resid, bf16 *out, const float *gamma, bf16 *norm_out, int *launches)
 {
     const hb_model_config &c = ctx->cfg;
     const int rows = launch_rows(T);
+    if (ctx->gemm_impl == 3) {
+        // whether the split-K kernel runs depends on the weight shape only
+        // (its first launch answers for all): a row's result does not depend
+        // on the batch it rides in
+        FastPath *f = ctx->fast;
+        cudaError_t e = cudaSuccess;
+        for (int t0 = 0; t0 < T && e == cudaSuccess; t0 += rows) {
+            const int Tn = T - t0 < rows ? T - t0 : rows;
+            e = launch_gemm_ksplit(M.m[kind], W, X + (size_t)t0 * K, Tn, N, K, resid + (size_t)t0 * N,
+                                   out + (size_t)t0 * N, gamma ? f->ss : nullptr, c.max_tokens, ctx->err_word, f->rt,
+                                   ctx->stream, true);
+            if (e == cudaErrorNotSupported && t0 == 0)
+                break;
+            *launches += 1;
+            if (e == cudaSuccess && gamma) {
+                e = launch_norm_apply(out + (size_t)t0 * N, f->ss, N / 128, c.max_tokens, gamma, c.rms_eps,
+                                      norm_out + (size_t)t0 * N, Tn, N, ctx->stream, true);
+                *launches += 1;
+            }
+        }
+        if (e != cudaErrorNotSupported)
+            return e;
+        cudaGetLastError();
+    }
     for (int t0 = 0; t0 < T; t0 += rows) {
         const int Tn = T - t0 < rows ? T - t0 : rows;
         EpiParams pp{};
@@ -305,7 +339,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
     const LayerMaps &M = ctx->fast->maps[l];
     const int T = b.T, H = c.hidden, d = c.head_dim;
     cudaStream_t s = ctx->stream;
-    const bool tc = ctx->gemm_impl == 2;
+    const bool tc = ctx->gemm_impl >= 2;
 
     // on the tensor-core path norm-1 of every layer but the first was
     // produced by the previous layer's final reduce
@@ -458,8 +492,8 @@ extern "C" int hb_set_kernels(hb_ctx *ctx, int gemm_impl, int attn_impl)
 {
     if (!ctx)
         return HB_EINVAL;
-    if ((gemm_impl != 0 && gemm_impl != 2) || attn_impl < 0 || attn_impl > 2)
-        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0 or 2, attn_impl 0, 1 or 2");
+    if ((gemm_impl != 0 && gemm_impl != 2 && gemm_impl != 3) || attn_impl < 0 || attn_impl > 2)
+        return ctx->set_error(HB_EINVAL, "hb_set_kernels: gemm_impl must be 0, 2 or 3, attn_impl 0, 1 or 2");
     ctx->gemm_impl = gemm_impl;
     ctx->attn_impl = attn_impl;
     return HB_OK;
@@ -471,8 +505,8 @@ extern "C" int hb_test_wait_timeout(hb_ctx *ctx, long long wait_ns)
         return HB_EINVAL;
     if (wait_ns < 100000 || wait_ns > 2000000000ll)
         return ctx->set_error(HB_EINVAL, "hb_test_wait_timeout: wait_ns must lie in [1e5, 2e9]");
-    if (ctx->gemm_impl != 2)
-        return ctx->set_error(HB_EINVAL, "hb_test_wait_timeout: needs the tensor-core GEMM (gemm_impl 2)");
+    if (ctx->gemm_impl < 2)
+        return ctx->set_error(HB_EINVAL, "hb_test_wait_timeout: needs the tensor-core GEMM (gemm_impl 2 or 3)");
     ctx->fast->fault_wait_ns = (uint64_t)wait_ns;
     return HB_OK;
 }

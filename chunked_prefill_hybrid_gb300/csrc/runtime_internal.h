@@ -103,7 +103,7 @@ struct hb_ctx {
 
     hb::Plan plan;
     hb::FastPath *fast = nullptr;
-    int gemm_impl = 2;  // 0: SIMT reference, 2: tcgen05 CTA pairs (2-SM MMA)
+    int gemm_impl = 2;  // 0: SIMT reference, 2: tcgen05 CTA pairs (2-SM MMA), 3: 2 + split-K clusters for O, down
     int attn_impl = 1;  // 0: simple, 1: paged attention (mma.sync chunk tiles), 2: tcgen05 chunk tiles
 
     // profiling and launch accounting

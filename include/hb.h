@@ -233,8 +233,12 @@ long long hb_launch_count(hb_ctx *ctx);
 int hb_gemm_test(hb_ctx *ctx, const void *X, const void *W, void *D, int T, int N, int K);
 
 /* Test hook: choose the kernels later calls use.  gemm_impl 0 = reference
- * SIMT GEMM, 2 = tcgen05 GEMM on CTA pairs with the 2-SM MMA (default; any
- * other value is HB_EINVAL); attn_impl 0 = one CTA per
+ * SIMT GEMM, 2 = tcgen05 GEMM on CTA pairs with the 2-SM MMA, the O and down
+ * projections stream-K into partials finished by a reduce pass (default), 3 =
+ * the same but O and down split K three ways inside 6-CTA clusters, summed
+ * through distributed shared memory with the residual fused (shapes whose
+ * clusters do not all fit at once fall back to 2); any other value is
+ * HB_EINVAL; attn_impl 0 = one CTA per
  * (row, head), 1 = paged attention with mma.sync chunk tiles (default), 2 =
  * paged attention with tcgen05 chunk tiles.  Every setting computes the same
  * function. */

@@ -77,7 +77,8 @@ def check_kv(ctx, w, pools, layer=0):
 # head_dim 128 and grouped-query shapes at a size the oracle finishes quickly
 D128 = synth.ModelDims(hidden=256, n_heads=2, n_kv_heads=2, head_dim=128, ffn=512)
 GQA = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn=384)
-KERNELS = {"pair+tcattn": (2, 2), "pair+hybrid": (2, 1), "pair+simple": (2, 0), "simt+hybrid": (0, 1)}
+KERNELS = {"ksplit+hybrid": (3, 1), "pair+tcattn": (2, 2), "pair+hybrid": (2, 1), "pair+simple": (2, 0),
+           "simt+hybrid": (0, 1)}
 
 
 def _tiny(seed, chunk_offset, chunk_len, ctxs, n_layers=1, gamma="ones", dims=synth.TINY):
@@ -120,7 +121,7 @@ def test_tiny_edge_cases(case, kern):
     ctx.free()
 
 
-@pytest.mark.parametrize("kern", ["pair+tcattn", "pair+hybrid", "pair+simple", "simt+hybrid"])
+@pytest.mark.parametrize("kern", ["ksplit+hybrid", "pair+tcattn", "pair+hybrid", "pair+simple", "simt+hybrid"])
 @pytest.mark.parametrize("dims", [D128, GQA], ids=["d128", "gqa"])
 @pytest.mark.parametrize("case", [
     ("hybrid", 200, 130, [0, 63, 64, 255, 256, 300, 1000]),
@@ -148,7 +149,7 @@ WIDE_FFN = synth.ModelDims(hidden=1024, n_heads=8, n_kv_heads=8, head_dim=128, f
 WIDE_FFN_SK = synth.ModelDims(hidden=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn=10240)
 
 
-@pytest.mark.parametrize("kern", ["pair+hybrid", "pair+tcattn"])
+@pytest.mark.parametrize("kern", ["ksplit+hybrid", "pair+hybrid", "pair+tcattn"])
 @pytest.mark.parametrize("dims", [WIDE_FFN, WIDE_FFN_SK], ids=["dp_wave", "stream_k"])
 @pytest.mark.parametrize("case", [(40, 90, [3, 200, 77, 500]), (0, 1, [])], ids=["hybrid", "one_row"])
 def test_wide_ffn_gate_up(case, dims, kern):
