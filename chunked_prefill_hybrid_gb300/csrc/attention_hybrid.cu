@@ -40,6 +40,12 @@ namespace {
 constexpr int CQ = 64;            // chunk tile rows
 constexpr int CK = 64;            // chunk key tile
 constexpr int NSTAGE = 8;         // decode ring depth (16-token blocks)
+// The four warps of a decode split take blocks round-robin, and ring slot s
+// holds blocks s, s + NSTAGE, s + 2 NSTAGE, ...: with NSTAGE a multiple of
+// four, one warp owns every block of a slot, so each slot's mbarrier phases
+// are waited for and refilled in order (a warp never waits on a phase two
+// ahead, which the parity test cannot tell from a completed one).
+static_assert(NSTAGE % 4 == 0, "decode ring depth must be a multiple of the four warps");
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
