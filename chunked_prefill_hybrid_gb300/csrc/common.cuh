@@ -128,6 +128,17 @@ struct EpiParams {
 
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// One rotate-half RoPE pair (x0 = feature i, x1 = feature i + d/2) turned by
+// the angle whose cosine and sine are (c, sn), with each product's rounding
+// fixed so every epilogue path gives the same bits.
+__device__ __forceinline__ void rope_rot(float &x0, float &x1, float c, float sn)
+{
+    const float a = __fmaf_rn(x0, c, -__fmul_rn(x1, sn));
+    const float b = __fmaf_rn(x1, c, __fmul_rn(x0, sn));
+    x0 = a;
+    x1 = b;
+}
+
 // One output pair (t, n..n+1), n even.
 __device__ __forceinline__ void epi_pair(const EpiParams &p, int t, int n, float a0, float a1)
 {
@@ -141,10 +152,7 @@ __device__ __forceinline__ void epi_pair(const EpiParams &p, int t, int n, float
         const int hb = n / d, i = (n % d) >> 1;
         if (hb < p.n_heads + p.n_kv) {
             const float2 cs = p.rope[(size_t)p.pos[t] * half + i];
-            const float x0 = a0 * cs.x - a1 * cs.y;
-            const float x1 = a1 * cs.x + a0 * cs.y;
-            a0 = x0;
-            a1 = x1;
+            rope_rot(a0, a1, cs.x, cs.y);
         }
         if (hb < p.n_heads) {
             bf16 *q = p.q_out + (size_t)t * p.n_heads * d + (size_t)hb * d;
@@ -244,12 +252,8 @@ __device__ __forceinline__ void epi_group_at(const EpiParams &p, int t, int n0, 
         if (hb < p.n_heads + p.n_kv) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 c = cs[k];
-                const float x0 = lo[2 * k], x1 = hi[2 * k], y0 = lo[2 * k + 1], y1 = hi[2 * k + 1];
-                lo[2 * k] = x0 * c.x - x1 * c.y;
-                hi[2 * k] = x1 * c.x + x0 * c.y;
-                lo[2 * k + 1] = y0 * c.z - y1 * c.w;
-                hi[2 * k + 1] = y1 * c.z + y0 * c.w;
+                rope_rot(lo[2 * k], hi[2 * k], cs[k].x, cs[k].y);
+                rope_rot(lo[2 * k + 1], hi[2 * k + 1], cs[k].z, cs[k].w);
             }
         }
         bf16 *base;

@@ -52,7 +52,8 @@ struct TcArgs {
     int *counters;    // [n_mtiles * G]
     const bf16 *w_tiled;  // the weights, streamed into L2 ahead of the TMA loads
     int rel;              // stages released per commit: 2 when the MMAs are short (N < 224), else 1
-    int qkv_smem;         // pair kernel, whole QKV tiles: stage the RoPE'd tile in shared memory, store coalesced
+    int qkv_smem;         // pair kernel, whole QKV tiles: 1 = stage the RoPE'd bf16 tile in shared memory, store
+                          // coalesced; 2 = dump the fp32 accumulator there, then rotate and store with every thread
     int dp_tiles;         // pair kernel: tile pairs 0..dp_tiles-1 go whole to clusters 0..dp_tiles-1 (fused
                           // epilogue); units / grid then cover only the stream-K rest, tile pairs dp_tiles..
     int slabs, slab_rows;  // token slabs of the launch (1: all T rows); slab s is rows s*slab_rows..
@@ -321,12 +322,8 @@ __device__ __forceinline__ void qkv_cols_to_smem(const EpiParams &p, const int *
         if (rot) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 cc = cs[k][q];
-                const float x0 = lo[2 * q], x1 = hi[2 * q], y0 = lo[2 * q + 1], y1 = hi[2 * q + 1];
-                lo[2 * q] = x0 * cc.x - x1 * cc.y;
-                hi[2 * q] = x1 * cc.x + x0 * cc.y;
-                lo[2 * q + 1] = y0 * cc.z - y1 * cc.w;
-                hi[2 * q + 1] = y1 * cc.z + y0 * cc.w;
+                rope_rot(lo[2 * q], hi[2 * q], cs[k][q].x, cs[k][q].y);
+                rope_rot(lo[2 * q + 1], hi[2 * q + 1], cs[k][q].z, cs[k][q].w);
             }
         }
         const uint32_t row = tile_s + 2u * (uint32_t)(c[k] * QKV_TS);
@@ -383,6 +380,115 @@ __device__ __forceinline__ void qkv_tile_out(const EpiParams &p, uint32_t s_slot
             asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(val[u].x), "r"(val[u].y),
                          "r"(val[u].z), "r"(val[u].w)
                          : "memory");
+        }
+    }
+}
+
+// QKV epilogue of a whole tile from its fp32 accumulator dumped to shared
+// memory, run by every thread of the CTA once the tensor-memory reads are
+// done (the producer and MMA warps are idle by then).
+//
+// The dump is feature-major: row f (one of the tile's 128 stored features,
+// RoPE pairs interleaved: even = head feature i, odd = feature i + d/2)
+// holds the tile's tokens as 16-byte chunks of 4 tokens, chunk c stored at
+// position c ^ ((f >> 4) & 7) (so within c's aligned group of 8: the row's
+// 8 * ceil(tg / 32) data chunks are permuted, never overlapped), and a row
+// is an odd number of chunks long.
+// An epilogue lane holds 32 tokens of one feature, so it writes 8 chunks;
+// the 8 lanes of a quarter-warp (8 consecutive features, one XOR) land on
+// 8 different bank groups because the row length is odd.  A reader thread
+// takes 4 tokens (one chunk) of the 16 features of a group g: the 8
+// quarter-warp lanes read the same chunk of the 8 groups, whose XORs differ,
+// so they too cover all 32 banks.  The reader then holds 8 RoPE pairs of 4
+// tokens; the 8 lanes of a token write its 128-byte lo and hi halves of a
+// head row, and read its 512-byte row of the (cos, sin) table.
+__host__ __device__ inline int qkv_dump_row_bytes(int tg) { return 16 * (8 * ((tg + 31) / 32) + 1); }
+
+__device__ __forceinline__ void qkv_dump_store(uint32_t dump_s, int row_bytes, int f, int col0, int ncol,
+                                               const uint32_t (&r)[32])
+{
+    const uint32_t row = dump_s + (uint32_t)(f * row_bytes);
+    const int x = (f >> 4) & 7, c0 = col0 >> 2;  // c -> c ^ x permutes each aligned group of 8 chunks
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (4 * j < ncol)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + 16u * (uint32_t)((c0 + j) ^ x)),
+                         "r"(r[4 * j]), "r"(r[4 * j + 1]), "r"(r[4 * j + 2]), "r"(r[4 * j + 3])
+                         : "memory");
+}
+
+__device__ __forceinline__ void qkv_dump_out(const EpiParams &p, const int *s_pos, const int *s_slot,
+                                             uint32_t dump_s, int row_bytes, int tile, int tid, int nthr)
+{
+    const int d = p.head_dim, half = d >> 1;
+    const int g = tid & 7;  // nthr % 8 == 0: a thread keeps its feature group
+    const int n0 = tile * TC_BM + 16 * g;
+    const int hb = n0 / d, i0 = (n0 % d) >> 1;
+    const int n_rot = p.n_heads + p.n_kv;
+    if (hb >= p.n_heads + 2 * p.n_kv)
+        return;  // rows past N
+    const bool is_q = hb < p.n_heads, rot = hb < n_rot;
+    const int kvh = rot ? hb - p.n_heads : hb - n_rot;
+    bf16 *const pool = (rot ? p.k_pool : p.v_pool) + (size_t)kvh * 16 * d + i0;
+    bf16 *const qcol = p.q_out + (size_t)hb * d + i0;
+    const float2 *const rope = p.rope + i0;
+    const uint32_t grow = dump_s + (uint32_t)(16 * g * row_bytes);
+    for (int tq = tid >> 3; 4 * tq < p.T; tq += nthr >> 3) {
+        float w[16][4];
+        const uint32_t cpos = 16u * (uint32_t)(tq ^ g);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(w[k][0]), "=f"(w[k][1]), "=f"(w[k][2]), "=f"(w[k][3])
+                         : "r"(grow + (uint32_t)(k * row_bytes) + cpos));
+        float4 cs[4][4];
+        int sl[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = 4 * tq + u;
+            sl[u] = 0;
+            if (t < p.T) {
+                if (!is_q)
+                    sl[u] = s_slot[t];
+                if (rot) {
+                    const float4 *src = reinterpret_cast<const float4 *>(rope + (size_t)s_pos[t] * half);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        cs[u][k] = __ldg(src + k);  // (cos, sin) of pairs 2k and 2k+1
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = 4 * tq + u;
+            if (t >= p.T)
+                continue;
+            float lo[8], hi[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                lo[k] = w[2 * k][u];
+                hi[k] = w[2 * k + 1][u];
+            }
+            if (rot) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    rope_rot(lo[2 * k], hi[2 * k], cs[u][k].x, cs[u][k].y);
+                    rope_rot(lo[2 * k + 1], hi[2 * k + 1], cs[u][k].z, cs[u][k].w);
+                }
+            }
+            bf16 *dst;
+            if (is_q) {
+                dst = qcol + (size_t)t * p.n_heads * d;
+            } else {
+                const int blk = sl[u] >> 4, off = sl[u] & 15;
+                if (blk < 0 || blk >= p.num_blocks) {
+                    set_dev_err(p.err, DERR_BAD_SLOT);
+                    continue;
+                }
+                dst = pool + ((size_t)blk * p.n_kv * 16 + off) * d;
+            }
+            *reinterpret_cast<uint4 *>(dst) = pack8_bf16(lo);
+            *reinterpret_cast<uint4 *>(dst + half) = pack8_bf16(hi);
         }
     }
 }
@@ -705,7 +811,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tmem_ld_wait();
                     const int col0 = sub * a.n_sub + c0;
                     const int ncol = min(32, a.n_sub - c0);
-                    if (staged) {
+                    if (staged && a.qkv_smem == 2) {
+                        qkv_dump_store(smem_u32(smem), qkv_dump_row_bytes(a.tg), f, col0, ncol, rr);
+                    } else if (staged) {
                         qkv_cols_to_smem(ep, s_pos, xp, col0, ncol, nb, tile, lane, rr, smem_u32(smem));
                     } else if (direct) {
                         emit_cols(ep, s_pos, s_slot, xp, 0, col0, ncol, nb, lane, rr);
@@ -722,7 +830,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if (lane == 0)
                     mbar_remote_arrive(sfree_leader + (uint32_t)(j * 8));
             }
-            if (staged) {
+            if (staged && a.qkv_smem == 1) {
                 epi_bar();  // the whole tile is in shared memory
                 qkv_tile_out(ep, smem_u32(s_slot), smem_u32(smem), tile, et);
             }
@@ -748,6 +856,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (a.qkv_smem == 2 && !*abort_flag) {
+        // the dumped tile (one whole tile pair per CTA pair): every thread
+        // rotates and stores; q and the KV pool may still be read by the
+        // previous kernel until it has completed
+        pdl_wait();
+        qkv_dump_out(ep, s_pos, s_slot, smem_u32(smem), qkv_dump_row_bytes(a.tg), 2 * (u0 / a.nkb) + r, threadIdx.x,
+                     TC_THREADS);
+    }
     cluster_sync();  // the leader's MMAs and both epilogues are done with both CTAs
     if (warp == 1) {
         tc_fence_after();
@@ -1015,10 +1131,11 @@ cudaError_t launch_gemm_pair(const CUtensorMap &tmW, const bf16 *W_tiled, const 
         if (n_mpairs > mc)
             return cudaErrorInvalidValue;
         a.grid = n_mpairs;
-        a.qkv_smem = (ep.mode == EPI_QKV && (ep.head_dim == 128 || ep.head_dim == 64) &&
-                      (long long)a.tg * QKV_TS * 2 <= (long long)stages * pair_stage_bytes(a.nsub, a.n_sub))
-                         ? 1
-                         : 0;
+        const long long stage_total = (long long)stages * pair_stage_bytes(a.nsub, a.n_sub);
+        if (ep.mode == EPI_QKV && (ep.head_dim == 128 || ep.head_dim == 64))
+            a.qkv_smem = (long long)TC_BM * qkv_dump_row_bytes(a.tg) <= stage_total ? 2
+                         : (long long)a.tg * QKV_TS * 2 <= stage_total   ? 1
+                                                                          : 0;
     }
     a.slots = tc_slots(units, a.grid, a.nkb);
     a.ws_slab = (size_t)a.grid * 2 * a.slots * a.tg * TC_BM;
