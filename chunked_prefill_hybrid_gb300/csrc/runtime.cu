@@ -701,12 +701,20 @@ static int async_setup(hb_ctx *ctx)
     const size_t bytes = (size_t)ctx->cfg.max_tokens * ctx->cfg.hidden * sizeof(bf16);
     int rc;
     if ((rc = ctx_alloc(ctx, (void **)&ctx->async_in[0], bytes)) ||
-        (rc = ctx_alloc(ctx, (void **)&ctx->async_in[1], bytes)))
+        (rc = ctx_alloc(ctx, (void **)&ctx->async_in[1], bytes)) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->async_out[0], bytes)) ||
+        (rc = ctx_alloc(ctx, (void **)&ctx->async_out[1], bytes)))
         return rc;
     for (int k = 0; k < 2; ++k)
         if (cudaEventCreateWithFlags(&ctx->in_ready[k], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ctx->in_free[k], cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&ctx->in_free[k], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ctx->out_free[k], cudaEventDisableTiming) != cudaSuccess)
             return ctx->set_error(HB_ECUDA, "cudaEventCreate failed");
+    // the output stream first: copy_stream marks a finished setup
+    if (cudaStreamCreateWithFlags(&ctx->out_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        ctx->out_stream = nullptr;
+        return ctx->set_error(HB_ECUDA, "cudaStreamCreate failed");
+    }
     if (cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
         ctx->copy_stream = nullptr;
         return ctx->set_error(HB_ECUDA, "cudaStreamCreate failed");
@@ -728,19 +736,18 @@ extern "C" int hb_forward_host_async(hb_ctx *ctx, const hb_batch_spec *spec, con
         return ctx->set_error(rc, "%s", e.c_str());
     if ((rc = async_setup(ctx)))
         return rc;
-    // the output must be page-locked memory the GPU can address (the last
-    // kernel writes it in place)
+    // the output must be page-locked, so that its copy is asynchronous
     cudaPointerAttributes pa{};
     if (cudaPointerGetAttributes(&pa, x_out_host) != cudaSuccess) {
         cudaGetLastError();
-        return ctx->set_error(HB_EINVAL, "x_out_host is not page-locked memory the GPU can address");
+        return ctx->set_error(HB_EINVAL, "x_out_host is not page-locked host memory");
     }
-    if (pa.type != cudaMemoryTypeHost || !pa.devicePointer || (uintptr_t)pa.devicePointer % 16 != 0)
-        return ctx->set_error(HB_EINVAL, "x_out_host must be 16-byte aligned page-locked memory the GPU can address");
-    void *y = pa.devicePointer;
-    // input slot k: its copy waits for the step that last read it, runs on
-    // the copy stream while the previous step computes, and the step waits
-    // for the copy
+    if (pa.type != cudaMemoryTypeHost)
+        return ctx->set_error(HB_EINVAL, "x_out_host is not page-locked host memory");
+    // slot k: the input copy waits for the step that last read input slot k
+    // and runs on the copy stream while the previous step computes; the step
+    // waits for it and for the copy that last read output slot k; the output
+    // copy follows the step on the output stream, beside the next step
     const int k = ctx->in_i ^= 1;
     const size_t bytes = (size_t)T * ctx->cfg.hidden * sizeof(bf16);
     if (ctx->in_used[k])
@@ -748,13 +755,18 @@ extern "C" int hb_forward_host_async(hb_ctx *ctx, const hb_batch_spec *spec, con
     CK(cudaMemcpyAsync(ctx->async_in[k], x_in_host, bytes, cudaMemcpyHostToDevice, ctx->copy_stream));
     CK(cudaEventRecord(ctx->in_ready[k], ctx->copy_stream));
     CK(cudaStreamWaitEvent(ctx->stream, ctx->in_ready[k], 0));
+    if (ctx->in_used[k])
+        CK(cudaStreamWaitEvent(ctx->stream, ctx->out_free[k], 0));
     BatchDev b;
-    if ((rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->async_in[k], y, b)) ||
-        (rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->async_in[k], y))) {
+    if ((rc = prepare_layers(ctx, spec, 0, ctx->cfg.n_layers, ctx->async_in[k], ctx->async_out[k], b)) ||
+        (rc = launch_layers(ctx, b, 0, ctx->cfg.n_layers, ctx->async_in[k], ctx->async_out[k]))) {
         cudaStreamSynchronize(ctx->stream);  // nothing of this call is left in flight
         return rc;
     }
     CK(cudaEventRecord(ctx->in_free[k], ctx->stream));
+    CK(cudaStreamWaitEvent(ctx->out_stream, ctx->in_free[k], 0));
+    CK(cudaMemcpyAsync(x_out_host, ctx->async_out[k], bytes, cudaMemcpyDeviceToHost, ctx->out_stream));
+    CK(cudaEventRecord(ctx->out_free[k], ctx->out_stream));
     ctx->in_used[k] = true;
     return HB_OK;
 }
@@ -766,6 +778,8 @@ extern "C" int hb_sync(hb_ctx *ctx)
     // the error word comes back on the stream, after its work: one wait
     CK(cudaMemcpyAsync(ctx->h_err, ctx->err_word, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
     CK(cudaStreamSynchronize(ctx->stream));
+    if (ctx->out_stream)
+        CK(cudaStreamSynchronize(ctx->out_stream));  // the asynchronous calls' output copies
     const int w = *ctx->h_err;
     if (w) {
         CK(cudaMemset(ctx->err_word, 0, sizeof(int)));
@@ -853,11 +867,17 @@ extern "C" void hb_free(hb_ctx *ctx)
         cudaStreamSynchronize(ctx->copy_stream);
         cudaStreamDestroy(ctx->copy_stream);
     }
+    if (ctx->out_stream) {
+        cudaStreamSynchronize(ctx->out_stream);
+        cudaStreamDestroy(ctx->out_stream);
+    }
     for (int k = 0; k < 2; ++k) {
         if (ctx->in_ready[k])
             cudaEventDestroy(ctx->in_ready[k]);
         if (ctx->in_free[k])
             cudaEventDestroy(ctx->in_free[k]);
+        if (ctx->out_free[k])
+            cudaEventDestroy(ctx->out_free[k]);
     }
     hb_free_fast_path(ctx);
     for (void *p : ctx->allocations)

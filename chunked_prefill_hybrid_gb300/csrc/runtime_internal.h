@@ -77,10 +77,14 @@ struct hb_ctx {
     hb::bf16 *xa = nullptr, *xb = nullptr, *host_in = nullptr, *host_out = nullptr;
     // hb_forward_host_async: a ring of two device input buffers filled on
     // copy_stream (in_ready[k] behind the copy, in_free[k] behind the step
-    // that read slot k), made on the first asynchronous call
+    // that read slot k) and a ring of two device output buffers, slot k
+    // copied to the caller's buffer on out_stream once its step is done
+    // (out_free[k] behind that copy); made on the first asynchronous call
     hb::bf16 *async_in[2] = {nullptr, nullptr};
-    cudaStream_t copy_stream = nullptr;
+    hb::bf16 *async_out[2] = {nullptr, nullptr};
+    cudaStream_t copy_stream = nullptr, out_stream = nullptr;
     cudaEvent_t in_ready[2] = {nullptr, nullptr}, in_free[2] = {nullptr, nullptr};
+    cudaEvent_t out_free[2] = {nullptr, nullptr};
     bool in_used[2] = {false, false};
     int in_i = 1;
     int *err_word = nullptr;

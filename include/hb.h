@@ -200,19 +200,22 @@ int hb_forward_host(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in_hos
  * shape: SARATHI summary, section 3.4, one hybrid batch per iteration).
  *   x_in_host:  host bf16 [T][hidden]; page-locked memory for an asynchronous
  *               copy.  It must stay unchanged until the next hb_sync.
- *   x_out_host: page-locked, 16-byte aligned host memory that the GPU can
- *               address (HB_EINVAL otherwise); the last kernel writes the
- *               result there in place.  Read it after hb_sync.
+ *   x_out_host: page-locked host memory (HB_EINVAL otherwise) for
+ *               [T][hidden] bf16.  Read it after hb_sync.
  * The input is copied into one of two device buffers on a second stream
  * while the previous batch computes; a buffer is refilled only after the
- * batch that read it.  Calls are ordered on the context's stream, like
- * hb_forward.  A batch rejected by the host checks returns the error with
+ * batch that read it.  The result goes to one of two device buffers and is
+ * copied to x_out_host on a third stream while the next batch computes; a
+ * batch reuses an output buffer only after its copy.  Calls are ordered on
+ * the context's stream, like hb_forward; hb_sync also waits for the output
+ * copies.  A batch rejected by the host checks returns the error with
  * nothing left in flight; device errors show at the next hb_sync.  The first
- * call makes the two input buffers (2 x max_tokens x hidden bf16), a stream
- * and four events. */
+ * call makes the two input and two output buffers (4 x max_tokens x hidden
+ * bf16), two streams and six events. */
 int hb_forward_host_async(hb_ctx *ctx, const hb_batch_spec *spec, const void *x_in_host, void *x_out_host);
 
-/* Wait for the context's stream; returns HB_EDEVICE if a kernel set the
+/* Wait for the context's stream and for the output copies of
+ * hb_forward_host_async; returns HB_EDEVICE if a kernel set the
  * device error word since the last hb_sync (and clears it). */
 int hb_sync(hb_ctx *ctx);
 
