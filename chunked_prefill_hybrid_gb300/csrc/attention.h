@@ -46,8 +46,10 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
                      int *n_chunk_items, int chunk_rows = 64);
 // Chunk tiles (mma.sync kernel, unless skip_chunk) then decode splits.
 // With skip_chunk the decode kernel follows a chunk kernel launched just
-// before it (launch_attention_chunk_tc).
-cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl = false, bool skip_chunk = false);
+// before it (launch_attention_chunk_tc).  tmK / tmV: make_tmap_kv_pool maps
+// of the layer's pools, which the decode splits load from.
+cudaError_t launch_attention_hybrid(const AttnParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                    cudaStream_t s, bool pdl = false, bool skip_chunk = false);
 
 // The chunk's attention on the tcgen05 tensor cores (attention_tc.cu):
 // 128-row tiles; tmK / tmV: make_tmap_kv_pool maps of the layer's pools.

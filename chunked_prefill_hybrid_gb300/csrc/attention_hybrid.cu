@@ -18,14 +18,16 @@
 //               ~16 significant bits.
 //   decode split one head of a single-row sequence over a range of its keys
 //               (1024..2047 keys; shorter contexts are one split).  Each
-//               16-token block of K and of V is one contiguous 4 KB run in
-//               the pool and is streamed with cp.async.bulk into
-//               an 8-stage shared-memory ring (mbarrier pipeline); 4 warps
-//               each take 4 tokens of a block, warp-shuffle dot products and
-//               an online softmax per warp.  The number of splits depends on
-//               the context length only.  Partial (m, l, o) go to a
-//               workspace; the last split to finish (per-(sequence, head)
-//               arrival counter, no waiting) merges them in split order.
+//               16-token block of K and of V is streamed by TMA (16-row x
+//               64-dim boxes, 128-byte swizzle) into an 8-stage shared-memory
+//               ring (mbarrier pipeline); the 4 warps take the blocks in turn,
+//               each with its own online softmax, and compute K q and V^T P
+//               on the tensor cores (mma.sync m16n8k16 with the query as the
+//               8-column side), merged across the warps at the end.  The
+//               number of splits depends on the context length only.
+//               Partial (m, l, o) go to a workspace; the last split to finish
+//               (per-(sequence, head) arrival counter, no waiting) merges
+//               them in split order.
 #include <cuda_runtime.h>
 
 #include "attention.h"
@@ -291,16 +293,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Lane that holds token t after the reduce-scatter below (and t of a lane).
-__device__ __forceinline__ int rs_lane_of(int t)
-{
-    return (((t >> 3) & 1) << 4) | (((t >> 2) & 1) << 3) | (((t >> 1) & 1) << 2) | ((t & 1) << 1);
-}
-__device__ __forceinline__ int rs_token_of(int lane)
-{
-    return (((lane >> 4) & 1) << 3) | (((lane >> 3) & 1) << 2) | (((lane >> 2) & 1) << 1) | ((lane >> 1) & 1);
-}
-
 // Keys [k0, k1) of split `split` of a sequence with nkeys keys: the splits
 // are near-equal, 16-aligned, and depend on nkeys alone.
 __device__ __forceinline__ void split_range(int nkeys, int split, int &k0, int &k1, int &n_splits)
@@ -311,17 +303,35 @@ __device__ __forceinline__ void split_range(int nkeys, int split, int &k0, int &
     k1 = min(nkeys, k0 + len);
 }
 
-// One warp takes a whole 16-token block: each lane forms partial dot
-// products of its E dims for all 16 tokens, a reduce-scatter across the
-// warp leaves token t's score in two lanes (16 shuffles per block), one
-// online-softmax step per block, and the weights are broadcast back for
-// the V accumulation.  Warp w handles blocks w, w+4, ...; it owns ring
-// stages w and w+4 and refills them itself, so no cross-warp handshake.
+// One decode split on the tensor cores, transposed so that the single query
+// is the 8-column side of each m16n8k16 product (7 of 8 columns padding,
+// rather than 15 of 16 rows):
+//   S^T[token] = K_block[token][:] . q      A = the block's K (16 tokens x
+//                16 dims per k-step), B column 0 = q (lanes 0-3 hold it);
+//   O^T[dim]  += V_block^T[dim][:] . P      A = V^T (ldmatrix .trans of the
+//                block's V), B column 0 = P (hi + lo bf16 parts, so the
+//                weights keep ~16 significant bits).
+// Column 0 of every product lands in the lanes with (lane & 3) == 0: lane
+// 4g holds tokens g and g + 8 of S^T, and dims 16 mt + g and 16 mt + g + 8
+// of O^T.  The ring's blocks arrive by TMA in 16-row x 64-dim boxes with the
+// 128-byte swizzle (16-byte chunk c of row r at c ^ (r & 7)), so every
+// ldmatrix is free of bank conflicts.  Warp w handles blocks w, w + 4, ...
+// with its own online softmax; it owns ring stages w and w + 4 and refills
+// them itself, so no cross-warp handshake until the final merge.
 template <int D>
-__device__ void decode_split(const AttnParams &p, int seq, int head, int split, uint8_t *smem)
+__device__ __forceinline__ uint32_t ring_addr(uint32_t block, int row, int chunk)
 {
-    constexpr int E = D / 32, BLK = 16 * D * 2, STG = 2 * BLK;
+    return block + (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+template <int D>
+__device__ void decode_split(const AttnParams &p, const CUtensorMap *tmK, const CUtensorMap *tmV, int seq, int head,
+                             int split, uint8_t *smem)
+{
+    constexpr int BLK = 16 * D * 2, STG = 2 * BLK;
+    constexpr int KS = D / 16;  // k-steps of S, m-tiles of O
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t4 = lane & 3;
     const int kvh = head / (p.n_heads / p.n_kv);
     const int row = p.b.seq_q0[seq];
     const int nkeys = p.b.seq_pos0[seq] + 1;
@@ -330,7 +340,7 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
     split_range(nkeys, split, k0, k1, n_splits);
     const int b0 = k0 >> 4, nb = ((k1 - 1) >> 4) - b0 + 1;
 
-    uint8_t *ring = smem;  // NSTAGE x (K block + V block)
+    uint8_t *ring = smem;  // NSTAGE x (K block + V block), 1024-byte aligned
     uint64_t *full = (uint64_t *)(smem + NSTAGE * STG);
     volatile int *flags = (volatile int *)(full + NSTAGE);  // [0] abort, [1] last
     float *red = (float *)(flags + 4);                      // [4][2 + D]
@@ -349,28 +359,35 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(kv_pol));
     auto issue = [&](int i) {
         const int s = i % NSTAGE;
-        const size_t off = (((size_t)bt[b0 + i] * p.n_kv + kvh) * 16) * D;
+        const int prow = (bt[b0 + i] * p.n_kv + kvh) * 16;  // the block's first row in the pool map
         mbar_expect_tx(&full[s], STG);
-        bulk_load_hint(ring + s * STG, p.k_pool + off, BLK, &full[s], kv_pol);
-        bulk_load_hint(ring + s * STG + BLK, p.v_pool + off, BLK, &full[s], kv_pol);
+#pragma unroll
+        for (int bx = 0; bx < D / 64; ++bx) {
+            tma_load_2d_hint(ring + s * STG + bx * 2048, tmK, &full[s], bx * 64, prow, kv_pol);
+            tma_load_2d_hint(ring + s * STG + BLK + bx * 2048, tmV, &full[s], bx * 64, prow, kv_pol);
+        }
     };
     if (lane == 0)
         for (int i = warp; i < min(nb, NSTAGE); i += 4)
             issue(i);
 
-    // q for this lane's E dims, pre-scaled into the log2 domain
-    const float sl2 = rsqrtf((float)D) * LOG2E;
-    float qv[E], acc[E];
+    // q as the B operand's column 0 (lanes 0-3), zero elsewhere
+    uint32_t qb[KS][2];
     {
-        const bf16 *qr = p.q + ((size_t)row * p.n_heads + head) * D + lane * E;
+        const unsigned int *qr =
+            reinterpret_cast<const unsigned int *>(p.q + ((size_t)row * p.n_heads + head) * D);
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-            qv[i] = bf2f(__ushort_as_bfloat16(__ldcg(reinterpret_cast<const unsigned short *>(qr + i)))) * sl2;
-            acc[i] = 0.f;
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = g == 0 ? __ldcg(qr + 8 * ks + t4) : 0u;
+            qb[ks][1] = g == 0 ? __ldcg(qr + 8 * ks + 4 + t4) : 0u;
         }
     }
+    const float sl2 = rsqrtf((float)D) * LOG2E;
+    float o[KS][4];
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt)
+        o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m = -INFINITY, l = 0.f;
-    const int my_tok = rs_token_of(lane);
     bool ok = true;
     for (int i = warp; i < nb; i += 4) {
         const int s = i % NSTAGE;
@@ -382,77 +399,76 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
             ok = false;
             break;
         }
-        const bf16 *Kb = reinterpret_cast<const bf16 *>(ring + s * STG) + lane * E;
-        const bf16 *Vb = reinterpret_cast<const bf16 *>(ring + s * STG + BLK) + lane * E;
-        float v[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            float d0 = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                d0 += qv[e] * bf2f(Kb[t * D + e]);
-            v[t] = d0;
+        const uint32_t kb = smem_u32(ring + s * STG), vb = kb + BLK;
+        // tokens of this block outside [k0, k1) (a slot that may never have
+        // been written): their V rows become zero, so that a weight of 0
+        // never meets a NaN, and their scores -inf
+        const int kbase = (b0 + i) * 16;
+        const int vlo = max(0, k0 - kbase), vhi = min(16, k1 - kbase);
+        if (vlo > 0 || vhi < 16) {
+            for (int c = lane; c < 16 * (D / 8); c += 32) {
+                const int r = c / (D / 8);
+                if (r < vlo || r >= vhi)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ring_addr<D>(vb, r, c % (D / 8))),
+                                 "r"(0)
+                                 : "memory");
+            }
+            __syncwarp();
         }
-        // reduce-scatter: 16 -> 8 -> 4 -> 2 -> 1 values, then pair sum
+        // S^T = K q
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const bool up = lane & 16;
-            const float send = up ? v[j] : v[8 + j];
-            const float keep = up ? v[8 + j] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        for (int ks = 0; ks < KS; ++ks) {
+            const int mi = lane >> 3;
+            const int r = (lane & 7) + (mi & 1) * 8, ch = 2 * ks + (mi >> 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(ring_addr<D>(kb, r, ch), a0, a1, a2, a3);
+            mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool up = lane & 8;
-            const float send = up ? v[j] : v[4 + j];
-            const float keep = up ? v[4 + j] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const bool up = lane & 4;
-            const float send = up ? v[j] : v[2 + j];
-            const float keep = up ? v[2 + j] : v[j];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        {
-            const bool up = lane & 2;
-            const float send = up ? v[0] : v[1];
-            const float keep = up ? v[1] : v[0];
-            v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-        float sc = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-        const int kp = (b0 + i) * 16 + my_tok;
-        if (kp < k0 || kp >= k1)
-            sc = -INFINITY;
-        float mx = sc;
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        // online softmax over the block's 16 tokens (lanes 4g: tokens g, g + 8)
+        float s0 = sc[0] * sl2, s1 = sc[2] * sl2;
+        if (kbase + g < k0 || kbase + g >= k1)
+            s0 = -INFINITY;
+        if (kbase + g + 8 < k0 || kbase + g + 8 >= k1)
+            s1 = -INFINITY;
+        float mx = fmaxf(s0, s1);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m, mx);  // finite: every block has a key in range
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(m, mx);  // finite in lanes 4g: every block has a key in range
         const float corr = exp2f(m - mn);
-        const float pw = exp2f(sc - mn);
-        float ps = (lane & 1) ? 0.f : pw;
-        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        const float p0 = exp2f(s0 - mn), p1 = exp2f(s1 - mn);
+        float ps = p0 + p1;
         ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 16);
         l = l * corr + ps;
         m = mn;
+        if (__any_sync(0xffffffffu, t4 == 0 && corr != 1.f)) {
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-            acc[e] *= corr;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            const float pt = __shfl_sync(0xffffffffu, pw, rs_lane_of(t));
-            // tokens outside [k0, k1) have weight 0 and may hold anything
-            // (a slot never written): leave them out rather than add 0 * v
-            if (pt > 0.f) {
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    acc[e] += pt * bf2f(Vb[t * D + e]);
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= corr;
+                o[mt][2] *= corr;
             }
+        }
+        // P as the B operand's column 0: lane t4 takes tokens 2 t4, 2 t4 + 1
+        // (from lanes 8 t4 and 8 t4 + 4) and 8 + 2 t4, 9 + 2 t4
+        const float h0 = __bfloat162float(__float2bfloat16_rn(p0)), h1 = __bfloat162float(__float2bfloat16_rn(p1));
+        const uint32_t hp = pack_bf16(h0, h1), lp = pack_bf16(p0 - h0, p1 - h1);
+        const int src = 8 * t4;
+        const uint32_t ha = __shfl_sync(0xffffffffu, hp, src), hb = __shfl_sync(0xffffffffu, hp, src + 4);
+        const uint32_t la = __shfl_sync(0xffffffffu, lp, src), lb = __shfl_sync(0xffffffffu, lp, src + 4);
+        const uint32_t bh0 = g == 0 ? __byte_perm(ha, hb, 0x5410) : 0u, bh1 = g == 0 ? __byte_perm(ha, hb, 0x7632) : 0u;
+        const uint32_t bl0 = g == 0 ? __byte_perm(la, lb, 0x5410) : 0u, bl1 = g == 0 ? __byte_perm(la, lb, 0x7632) : 0u;
+        // O^T += V^T P
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int mi = lane >> 3;
+            const int r = (lane & 7) + (mi >> 1) * 8, ch = 2 * mt + (mi & 1);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(ring_addr<D>(vb, r, ch), a0, a1, a2, a3);
+            mma16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+            mma16816(o[mt], a0, a1, a2, a3, bl0, bl1);
         }
         // this warp is the only reader of stage s: refill it
         if (i + NSTAGE < nb) {
@@ -468,9 +484,13 @@ __device__ void decode_split(const AttnParams &p, int seq, int head, int split, 
         red[warp * (2 + D) + 0] = m;
         red[warp * (2 + D) + 1] = l;
     }
+    if (t4 == 0) {
 #pragma unroll
-    for (int e = 0; e < E; ++e)
-        red[warp * (2 + D) + 2 + lane * E + e] = acc[e];
+        for (int mt = 0; mt < KS; ++mt) {
+            red[warp * (2 + D) + 2 + 16 * mt + g] = o[mt][0];
+            red[warp * (2 + D) + 2 + 16 * mt + g + 8] = o[mt][2];
+        }
+    }
     __syncthreads();
     if (!ok || flags[0]) {
         // let the copies already issued land before the CTA exits
@@ -564,7 +584,9 @@ __global__ void __launch_bounds__(128) k_attention_chunk(AttnParams p)
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) k_attention_decode(AttnParams p, int wait_first)
+__global__ void __launch_bounds__(128) k_attention_decode(const __grid_constant__ CUtensorMap tmK,
+                                                          const __grid_constant__ CUtensorMap tmV, AttnParams p,
+                                                          int wait_first)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -574,7 +596,7 @@ __global__ void __launch_bounds__(128) k_attention_decode(AttnParams p, int wait
     const int item = p.n_chunk_items + blockIdx.x / p.n_heads;
     const int head = blockIdx.x % p.n_heads;
     if (item < p.n_items)
-        decode_split<D>(p, p.items[2 * item], head, p.items[2 * item + 1], smem);
+        decode_split<D>(p, &tmK, &tmV, p.items[2 * item], head, p.items[2 * item + 1], smem);
     else if (threadIdx.x == 0)
         set_dev_err(p.err, DERR_BAD_WORK);
     if (!wait_first && blockIdx.x == gridDim.x - 1)
@@ -624,7 +646,8 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
 }
 
 template <int D>
-static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool pdl, bool skip_chunk)
+static cudaError_t launch_attention_d(const AttnParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                      cudaStream_t s, bool pdl, bool skip_chunk)
 {
     static bool configured = false;
     const int cs = chunk_smem_bytes(D), ds = decode_smem_bytes(D);
@@ -648,21 +671,22 @@ static cudaError_t launch_attention_d(const AttnParams &p, cudaStream_t s, bool 
         // waits at its end; alone, it waits for the QKV projection first
         const int wait_first = (p.n_chunk_items > 0 && pdl) ? 0 : 1;
         cudaError_t e = launch_kernel(pdl, k_attention_decode<D>, dim3(n_dec * p.n_heads), dim3(128), (size_t)ds, s,
-                                      p, wait_first);
+                                      tmK, tmV, p, wait_first);
         if (e != cudaSuccess)
             return e;
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention_hybrid(const AttnParams &p, cudaStream_t s, bool pdl, bool skip_chunk)
+cudaError_t launch_attention_hybrid(const AttnParams &p, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                                    cudaStream_t s, bool pdl, bool skip_chunk)
 {
     if (p.n_items <= 0)
         return cudaSuccess;
     if (p.head_dim == 128)
-        return launch_attention_d<128>(p, s, pdl, skip_chunk);
+        return launch_attention_d<128>(p, tmK, tmV, s, pdl, skip_chunk);
     if (p.head_dim == 64)
-        return launch_attention_d<64>(p, s, pdl, skip_chunk);
+        return launch_attention_d<64>(p, tmK, tmV, s, pdl, skip_chunk);
     return cudaErrorInvalidValue;
 }
 

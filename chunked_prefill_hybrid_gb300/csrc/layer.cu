@@ -207,7 +207,7 @@ static cudaError_t launch_attention_tc(const AttnParams &ap, const CUtensorMap &
     cudaError_t e = launch_attention_chunk_tc(ap, tmK, tmV, s, pdl);
     if (e != cudaSuccess)
         return e;
-    return launch_attention_hybrid(ap, s, pdl, true);
+    return launch_attention_hybrid(ap, tmK, tmV, s, pdl, true);
 }
 
 // The epilogue parameters of stored output features [n1, N) of a product
@@ -390,7 +390,7 @@ int run_layer(hb_ctx *ctx, int l, int l_first, int l_last, const BatchDev &b, co
         if (ctx->attn_impl == 2)
             LK(K_ATTENTION, launch_attention_tc(ap, f->kv_maps[2 * l], f->kv_maps[2 * l + 1], s, pdl));
         else
-            LK(K_ATTENTION, launch_attention_hybrid(ap, s, pdl));
+            LK(K_ATTENTION, launch_attention_hybrid(ap, f->kv_maps[2 * l], f->kv_maps[2 * l + 1], s, pdl));
         // LK counted one: the chunk tiles and the decode splits are separate kernels
         if (f->n_chunk_items > 0 && f->n_items > f->n_chunk_items)
             ctx->n_launches++;
