@@ -30,6 +30,9 @@
 //               them in split order.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "attention.h"
 #include "tc_ptx.cuh"
 
@@ -630,6 +633,7 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
             }
     *n_chunk_items = n;
     int off = 0;
+    const int d0 = n;
     for (int s = 0; s < n_seq; ++s) {
         part_off[s] = off;
         if (seq_nq[s] == 1) {
@@ -642,6 +646,24 @@ int attn_build_items(const int *seq_nq, const int *seq_pos0, int n_seq, int *ite
             off += ns;
         }
     }
+    // the decode splits longest first, so that a long split does not start
+    // last and stretch the kernel's tail (stable: equal lengths keep their
+    // order; a split's result and the merge order do not depend on this)
+    auto split_keys = [&](int i) {
+        const int nk = seq_pos0[items[2 * i]] + 1;
+        const int len = attn_split_len(nk);
+        return std::min(nk, (items[2 * i + 1] + 1) * len) - items[2 * i + 1] * len;
+    };
+    std::vector<int> order(n - d0);
+    for (int i = 0; i < n - d0; ++i)
+        order[i] = d0 + i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return split_keys(a) > split_keys(b); });
+    std::vector<int> sorted(2 * (n - d0));
+    for (int i = 0; i < n - d0; ++i) {
+        sorted[2 * i] = items[2 * order[i]];
+        sorted[2 * i + 1] = items[2 * order[i] + 1];
+    }
+    std::copy(sorted.begin(), sorted.end(), items + 2 * d0);
     return n;
 }
 
