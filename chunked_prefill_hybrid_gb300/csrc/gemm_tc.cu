@@ -172,6 +172,49 @@ __device__ __forceinline__ void emit_cols(const EpiParams &p, const int *s_pos, 
         }
         return;
     }
+    if (p.mode == EPI_SWIGLU) {
+        // feature-major staging in 16-byte chunks of 4 tokens, chunk c of
+        // feature f at c ^ (f & 7): lane f writes its 32 tokens as 8 chunks,
+        // then lane (tq, o) reads 4 tokens (chunk tq) of features 8o..8o+7,
+        // i.e. 4 (gate, up) pairs, and writes 4 act values per token; both
+        // sides cover all 32 banks per quarter-warp
+        const uint32_t xs = smem_u32(xp);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xs + 128u * (uint32_t)lane +
+                                                                           16u * (uint32_t)(c ^ (lane & 7))),
+                         "r"(r[4 * c]), "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
+                         : "memory");
+        __syncwarp();
+        const int tq = lane & 7, o = lane >> 3;
+        float w[8][4];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(w[k][0]), "=f"(w[k][1]), "=f"(w[k][2]), "=f"(w[k][3])
+                         : "r"(xs + 128u * (uint32_t)(8 * o + k) + 16u * (uint32_t)(tq ^ k)));
+        __syncwarp();
+        const int j0 = (nb + 8 * o) >> 1;  // act feature of this lane's first pair
+        if (j0 < p.ffn) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = col0 + 4 * tq + u;
+                if (4 * tq + u < ncol && t_base + c < p.T) {
+                    float a[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        a[k] = silu_f(w[2 * k][u]) * w[2 * k + 1][u];
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(a[0], a[1]), h1 = __floats2bfloat162_rn(a[2], a[3]);
+                    uint2 v;
+                    v.x = *reinterpret_cast<uint32_t *>(&h0);
+                    v.y = *reinterpret_cast<uint32_t *>(&h1);
+                    *reinterpret_cast<uint2 *>(p.act + (size_t)(t_base + c) * p.ffn + j0) = v;
+                }
+            }
+        }
+        return;
+    }
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 32; ++j)
