@@ -114,9 +114,10 @@ __global__ void __launch_bounds__(TWO ? 640 : 1024, TWO ? 2 : 1) k_reduce_norm(R
     float o[8];
     float ss = 0.f;
     if (n0 < a.N) {
+        // the residual's load goes out with the partials' first round
+        const uint4 rv = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
         float acc[8];
         rd_sum<8, TWO ? 2 : 4>(p, tab, t, n0, acc);
-        const uint4 rv = *reinterpret_cast<const uint4 *>(a.resid + (size_t)t * a.N + n0);
         const bf16 *re = reinterpret_cast<const bf16 *>(&rv);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
