@@ -321,7 +321,8 @@ __device__ __forceinline__ void split_range(int nkeys, int split, int &k0, int &
 // ldmatrix is free of bank conflicts.  Warp w handles blocks w, w + 4, ...
 // with its own online softmax; it owns ring stages w and w + 4 and refills
 // them itself, so no cross-warp handshake until the final merge.
-template <int D>
+// Shared-memory address of (row, 16-byte chunk) of a ring block stored as
+// 2048-byte boxes of 16 rows x 128 bytes (64 dims) with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t ring_addr(uint32_t block, int row, int chunk)
 {
     return block + (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
@@ -412,7 +413,7 @@ __device__ void decode_split(const AttnParams &p, const CUtensorMap *tmK, const 
             for (int c = lane; c < 16 * (D / 8); c += 32) {
                 const int r = c / (D / 8);
                 if (r < vlo || r >= vhi)
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ring_addr<D>(vb, r, c % (D / 8))),
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(ring_addr(vb, r, c % (D / 8))),
                                  "r"(0)
                                  : "memory");
             }
@@ -425,7 +426,7 @@ __device__ void decode_split(const AttnParams &p, const CUtensorMap *tmK, const 
             const int mi = lane >> 3;
             const int r = (lane & 7) + (mi & 1) * 8, ch = 2 * ks + (mi >> 1);
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(ring_addr<D>(kb, r, ch), a0, a1, a2, a3);
+            ldsm_x4(ring_addr(kb, r, ch), a0, a1, a2, a3);
             mma16816(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
         }
         // online softmax over the block's 16 tokens (lanes 4g: tokens g, g + 8)
@@ -469,7 +470,7 @@ __device__ void decode_split(const AttnParams &p, const CUtensorMap *tmK, const 
             const int mi = lane >> 3;
             const int r = (lane & 7) + (mi >> 1) * 8, ch = 2 * mt + (mi & 1);
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(ring_addr<D>(vb, r, ch), a0, a1, a2, a3);
+            ldsm_x4_t(ring_addr(vb, r, ch), a0, a1, a2, a3);
             mma16816(o[mt], a0, a1, a2, a3, bh0, bh1);
             mma16816(o[mt], a0, a1, a2, a3, bl0, bl1);
         }
