@@ -19,6 +19,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <string>
 #include <vector>
 
@@ -698,20 +699,21 @@ static int async_setup(hb_ctx *ctx)
 {
     if (ctx->copy_stream)
         return HB_OK;
+    // each piece is made once, so that a setup that failed part-way can be
+    // retried by the next call without leaking what it had made
     const size_t bytes = (size_t)ctx->cfg.max_tokens * ctx->cfg.hidden * sizeof(bf16);
     int rc;
-    if ((rc = ctx_alloc(ctx, (void **)&ctx->async_in[0], bytes)) ||
-        (rc = ctx_alloc(ctx, (void **)&ctx->async_in[1], bytes)) ||
-        (rc = ctx_alloc(ctx, (void **)&ctx->async_out[0], bytes)) ||
-        (rc = ctx_alloc(ctx, (void **)&ctx->async_out[1], bytes)))
-        return rc;
-    for (int k = 0; k < 2; ++k)
-        if (cudaEventCreateWithFlags(&ctx->in_ready[k], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ctx->in_free[k], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ctx->out_free[k], cudaEventDisableTiming) != cudaSuccess)
+    for (bf16 **buf : {&ctx->async_in[0], &ctx->async_in[1], &ctx->async_out[0], &ctx->async_out[1]})
+        if (!*buf && (rc = ctx_alloc(ctx, (void **)buf, bytes)))
+            return rc;
+    for (cudaEvent_t *ev : {&ctx->in_ready[0], &ctx->in_ready[1], &ctx->in_free[0], &ctx->in_free[1],
+                            &ctx->out_free[0], &ctx->out_free[1]})
+        if (!*ev && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) != cudaSuccess) {
+            *ev = nullptr;
             return ctx->set_error(HB_ECUDA, "cudaEventCreate failed");
+        }
     // the output stream first: copy_stream marks a finished setup
-    if (cudaStreamCreateWithFlags(&ctx->out_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    if (!ctx->out_stream && cudaStreamCreateWithFlags(&ctx->out_stream, cudaStreamNonBlocking) != cudaSuccess) {
         ctx->out_stream = nullptr;
         return ctx->set_error(HB_ECUDA, "cudaStreamCreate failed");
     }
